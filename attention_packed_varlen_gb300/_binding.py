@@ -1,0 +1,243 @@
+"""Thin ctypes binding of the C ABI in ``include/slm_attn.h``.
+
+Argument marshalling only: tensors are checked for device, dtype, shape and
+contiguity, their device pointers and the current CUDA stream are handed to
+the library, and every step of the computation runs in its CUDA kernels.
+There is no fallback: if the library is missing or fails to load, calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libslm_attn.so")
+
+SLM_OK = 0
+STATUS_NAMES = {0: "SLM_OK", 1: "SLM_ERR_INVALID_ARG", 2: "SLM_ERR_UNSUPPORTED", 3: "SLM_ERR_CUDA",
+                4: "SLM_ERR_WORKSPACE", 5: "SLM_ERR_DEVICE_CHECK"}
+
+EXPORTS = ("slm_last_error", "slm_abi_version", "slm_packed_prefill_attn", "slm_prefill_workspace_size",
+           "slm_shared_prefix_decode_attn", "slm_beam_select", "slm_beam_select_workspace_size",
+           "slm_check_status")
+
+
+class SlmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Loads the CUDA library (built by ``attention_packed_varlen_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} is missing "
+                               "(run `python -m attention_packed_varlen_gb300.build`)")
+        lib = ctypes.CDLL(p)
+        P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        lib.slm_last_error.restype = ctypes.c_char_p
+        lib.slm_last_error.argtypes = []
+        lib.slm_abi_version.restype = i32
+        lib.slm_abi_version.argtypes = []
+        lib.slm_packed_prefill_attn.restype = ctypes.c_int
+        lib.slm_packed_prefill_attn.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, sz, P, P]
+        lib.slm_prefill_workspace_size.restype = sz
+        lib.slm_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.slm_shared_prefix_decode_attn.restype = ctypes.c_int
+        lib.slm_shared_prefix_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                      f32, P, P, P, P, P, P]
+        lib.slm_beam_select.restype = ctypes.c_int
+        lib.slm_beam_select.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P, P, P, sz, P]
+        lib.slm_beam_select_workspace_size.restype = sz
+        lib.slm_beam_select_workspace_size.argtypes = [i32, i32, i32]
+        lib.slm_check_status.restype = ctypes.c_int
+        lib.slm_check_status.argtypes = [P, P]
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != SLM_OK:
+        raise SlmError(status, load().slm_last_error().decode(errors="replace"))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, dim: Optional[int] = None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dimensions, got {t.dim()}")
+
+
+# ----------------------------------------------------------------------------
+# Size queries
+# ----------------------------------------------------------------------------
+def slm_prefill_workspace_size(num_seqs: int, total_tokens: int, max_seqlen: int, n_q_heads: int,
+                               n_kv_heads: int) -> int:
+    return int(load().slm_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, n_q_heads, n_kv_heads))
+
+
+def slm_beam_select_workspace_size(W_in: int, V: int, W: int) -> int:
+    return int(load().slm_beam_select_workspace_size(W_in, V, W))
+
+
+def slm_abi_version() -> int:
+    return int(load().slm_abi_version())
+
+
+# ----------------------------------------------------------------------------
+# Packed prefill
+# ----------------------------------------------------------------------------
+def slm_packed_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                            max_seqlen: int, softmax_scale: Optional[float] = None, *,
+                            cu_seqlens_host: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                            lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """O [T, Hq, D] of packed causal GQA attention over sequences delimited by
+    ``cu_seqlens`` (int32 [B+1], on the device).  ``lse`` (fp32 [Hq, T]) is
+    filled when given."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    if k.shape != (T, Hkv, D) or v.shape != (T, Hkv, D):
+        raise ValueError("k and v must be [T, Hkv, D] matching q")
+    B = cu_seqlens.shape[0] - 1
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    need = slm_prefill_workspace_size(B, T, int(max_seqlen), Hq, Hkv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    host_cs = None
+    if cu_seqlens_host is not None:
+        host_cs = cu_seqlens_host.to(torch.int32).contiguous()
+        if host_cs.is_cuda:
+            raise ValueError("cu_seqlens_host must be on the CPU")
+    st = load().slm_packed_prefill_attn(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(host_cs), B, T, int(max_seqlen), Hq, Hkv, D, scale,
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(q.device))
+    _check(st)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Shared-prefix decode
+# ----------------------------------------------------------------------------
+def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], vp: Optional[torch.Tensor],
+                                  ks: Optional[torch.Tensor], vs: Optional[torch.Tensor],
+                                  k_new: Optional[torch.Tensor], v_new: Optional[torch.Tensor],
+                                  parent_idx: Optional[torch.Tensor], L_prev: int,
+                                  softmax_scale: Optional[float] = None, *, ks_out: torch.Tensor,
+                                  vs_out: torch.Tensor, out: Optional[torch.Tensor] = None,
+                                  lse: Optional[torch.Tensor] = None,
+                                  dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """O [W, Hq, D] of beam decode attention over the shared prompt K/V plus
+    each beam's reordered suffix; writes the reordered suffix to ks_out/vs_out."""
+    _need(q, "q", torch.bfloat16, 3)
+    W, Hq, D = q.shape
+    _need(ks_out, "ks_out", torch.bfloat16, 4)
+    _need(vs_out, "vs_out", torch.bfloat16, 4)
+    Smax, Hkv = ks_out.shape[1], ks_out.shape[2]
+    Lp = 0
+    if kp is not None:
+        _need(kp, "kp", torch.bfloat16, 3)
+        _need(vp, "vp", torch.bfloat16, 3)
+        Lp = kp.shape[0]
+        if kp.shape != (Lp, Hkv, D) or vp.shape != kp.shape:
+            raise ValueError("kp/vp must be [Lp, Hkv, D]")
+    for name, t in (("ks", ks), ("vs", vs)):
+        if t is not None:
+            _need(t, name, torch.bfloat16, 4)
+            if t.shape != (W, Smax, Hkv, D):
+                raise ValueError(f"{name} must be [W, Smax, Hkv, D]")
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t is not None:
+            _need(t, name, torch.bfloat16, 3)
+            if t.shape != (W, Hkv, D):
+                raise ValueError(f"{name} must be [W, Hkv, D]")
+    if parent_idx is not None:
+        _need(parent_idx, "parent_idx", torch.int32, 1)
+    scale = float(softmax_scale) if softmax_scale is not None else 1.0 / float(D) ** 0.5
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, 2)
+    st = load().slm_shared_prefix_decode_attn(
+        _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(k_new), _ptr(v_new), _ptr(parent_idx), W, Lp,
+        int(L_prev), Smax, Hq, Hkv, D, scale, _ptr(ks_out), _ptr(vs_out), _ptr(out), _ptr(lse), _ptr(dev_status),
+        _stream(q.device))
+    _check(st)
+    return out
+
+
+# ----------------------------------------------------------------------------
+# Beam selection
+# ----------------------------------------------------------------------------
+def slm_beam_select(logits: torch.Tensor, cum_scores: torch.Tensor, W: int, *, workspace=None,
+                    want_candidates: bool = True, want_lse: bool = True):
+    """Returns dict(token, parent, score [W]; cand_token, cand_parent,
+    cand_score [2W]; lse [W_in])."""
+    _need(logits, "logits", torch.bfloat16, 2)
+    _need(cum_scores, "cum_scores", torch.float32, 1)
+    W_in, V = logits.shape
+    dev = logits.device
+    need = slm_beam_select_workspace_size(W_in, V, W)
+    if need == 0:
+        raise SlmError(2, f"unsupported beam sizes W_in={W_in} V={V} W={W}")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    res = {
+        "token": torch.empty(W, dtype=torch.int32, device=dev),
+        "parent": torch.empty(W, dtype=torch.int32, device=dev),
+        "score": torch.empty(W, dtype=torch.float32, device=dev),
+    }
+    if want_candidates:
+        res["cand_token"] = torch.empty(2 * W, dtype=torch.int32, device=dev)
+        res["cand_parent"] = torch.empty(2 * W, dtype=torch.int32, device=dev)
+        res["cand_score"] = torch.empty(2 * W, dtype=torch.float32, device=dev)
+    if want_lse:
+        res["lse"] = torch.empty(W_in, dtype=torch.float32, device=dev)
+    st = load().slm_beam_select(
+        _ptr(logits), _ptr(cum_scores), W_in, V, W, _ptr(res["token"]), _ptr(res["parent"]), _ptr(res["score"]),
+        _ptr(res.get("cand_token")), _ptr(res.get("cand_parent")), _ptr(res.get("cand_score")), _ptr(res.get("lse")),
+        _ptr(workspace), workspace.numel(), _stream(dev))
+    _check(st)
+    return res
+
+
+def slm_check_status(dev_status: torch.Tensor) -> None:
+    _need(dev_status, "dev_status", torch.int32)
+    _check(load().slm_check_status(_ptr(dev_status), _stream(dev_status.device)))

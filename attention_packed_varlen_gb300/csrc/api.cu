@@ -1,0 +1,381 @@
+// C ABI of the attention hot path (declared in include/slm_attn.h): argument
+// validation, TMA tensor-map encoding, schedule and kernel launches.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn_tc.cuh"
+#include "slm_attn.h"
+#include "slm_internal.h"
+
+namespace slm {
+
+// Defined in beam_select.cu
+size_t beam_select_workspace_bytes(int W_in, int V, int W);
+bool beam_select_supported(int W_in, int V, int W);
+cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, int V, int W, int32_t* out_token,
+                               int32_t* out_parent, float* out_score, int32_t* out_cand_token,
+                               int32_t* out_cand_parent, float* out_cand_score, float* out_lse, void* workspace,
+                               cudaStream_t stream);
+
+namespace {
+
+thread_local std::string g_last_error;
+
+slm_status fail(slm_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+slm_status ok() {
+  g_last_error.clear();
+  return SLM_OK;
+}
+
+slm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SLM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- TMA descriptor encoding through the driver entry point ----------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<EncodeTiledFn>(nullptr);
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// bf16 tensor [d2, d1, d0] (d0 contiguous), 128-byte swizzled boxes
+// {64, box1, box2}; out-of-range elements read as zero.
+bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box1,
+                    uint32_t box2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {64, box1, box2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, AttnMode MODE>
+cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
+                        int grid_x, cudaStream_t stream) {
+  auto kern = attn_tc_kernel<D, MODE>;
+  const int smem = SmemLayout<D>::kAlloc;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid_x, kThreads, smem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+// ---- prefill tile schedule -------------------------------------------------
+constexpr int kSchedThreads = 1024;
+constexpr int kMaxKvBlocks = 4095;  // longest sequence: 4095 * 128 tokens
+constexpr int kBuckets = 4096;
+
+// Lists the (sequence, query tile) work items, heaviest first (number of
+// 128-key blocks a tile reads, descending), after checking the boundary.
+__global__ void __launch_bounds__(kSchedThreads)
+    prefill_schedule_kernel(const int32_t* cu, int B, int T, int tok, int max_nb, int32_t* tiles,
+                            int32_t* dev_status) {
+  __shared__ int cnt[kBuckets];
+  __shared__ int warp_tot[kSchedThreads / 32];
+  __shared__ int bad;
+  for (int i = threadIdx.x; i < kBuckets; i += kSchedThreads) cnt[i] = 0;
+  if (threadIdx.x == 0) bad = (cu[0] != 0 || cu[B] != T) ? 1 : 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += kSchedThreads) {
+    const int len = cu[b + 1] - cu[b];
+    if (len < 0 || (len + kBlockN - 1) / kBlockN > max_nb) bad = 1;
+  }
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      tiles[0] = 0;
+      if (dev_status) atomicOr(dev_status, kDevBadSeqlens);
+    }
+    return;
+  }
+  for (int b = threadIdx.x; b < B; b += kSchedThreads) {
+    const int len = cu[b + 1] - cu[b];
+    const int nt = (len + tok - 1) / tok;
+    for (int qt = 0; qt < nt; ++qt) atomicAdd(&cnt[(min(len, (qt + 1) * tok) + kBlockN - 1) / kBlockN], 1);
+  }
+  __syncthreads();
+  // exclusive scan from the heaviest bucket down: 4 buckets per thread
+  int loc[4], s = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    loc[i] = cnt[kBuckets - 1 - (4 * threadIdx.x + i)];
+    s += loc[i];
+  }
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = s;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[w] = x;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int i = 0; i < kSchedThreads / 32; ++i) {
+    if (i < w) base += warp_tot[i];
+    total += warp_tot[i];
+  }
+  int run = base + x - s;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    cnt[kBuckets - 1 - (4 * threadIdx.x + i)] = run;
+    run += loc[i];
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += kSchedThreads) {
+    const int len = cu[b + 1] - cu[b];
+    const int nt = (len + tok - 1) / tok;
+    for (int qt = 0; qt < nt; ++qt) {
+      const int pos = atomicAdd(&cnt[(min(len, (qt + 1) * tok) + kBlockN - 1) / kBlockN], 1);
+      tiles[1 + 2 * pos] = b;
+      tiles[2 + 2 * pos] = qt;
+    }
+  }
+  if (threadIdx.x == 0) tiles[0] = total;
+}
+
+int64_t prefill_tile_capacity(int32_t num_seqs, int32_t total_tokens, int32_t tok) {
+  return static_cast<int64_t>(total_tokens) / tok + num_seqs + 1;
+}
+
+}  // namespace
+}  // namespace slm
+
+using namespace slm;
+
+extern "C" {
+
+const char* slm_last_error(void) { return g_last_error.c_str(); }
+
+int32_t slm_abi_version(void) { return 1; }
+
+size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t n_q_heads,
+                                  int32_t n_kv_heads) {
+  (void)max_seqlen;
+  if (num_seqs < 0 || total_tokens < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return 0;
+  const int G = n_q_heads / n_kv_heads;
+  if (G > kBlockM) return 0;
+  const int64_t cap = prefill_tile_capacity(num_seqs, total_tokens, kBlockM / G);
+  return static_cast<size_t>(((1 + 2 * cap) * 4 + 255) / 256 * 256);
+}
+
+slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                   const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens,
+                                   int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                   float softmax_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0)
+    return fail(SLM_ERR_INVALID_ARG, "negative size (num_seqs=%d total_tokens=%d max_seqlen=%d)", num_seqs,
+                total_tokens, max_seqlen);
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
+    return fail(SLM_ERR_INVALID_ARG, "need n_q_heads %% n_kv_heads == 0 (got %d, %d)", n_q_heads, n_kv_heads);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(SLM_ERR_UNSUPPORTED, "head_dim %d unsupported (64 or 128)", head_dim);
+  const int G = n_q_heads / n_kv_heads;
+  if (G > kBlockM) return fail(SLM_ERR_UNSUPPORTED, "query heads per KV head %d > %d", G, kBlockM);
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return fail(SLM_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if ((max_seqlen + kBlockN - 1) / kBlockN > kMaxKvBlocks)
+    return fail(SLM_ERR_UNSUPPORTED, "max_seqlen %d above %d", max_seqlen, kMaxKvBlocks * kBlockN);
+  if (cu_seqlens_host) {
+    if (cu_seqlens_host[0] != 0 || cu_seqlens_host[num_seqs] != total_tokens)
+      return fail(SLM_ERR_INVALID_ARG, "cu_seqlens must start at 0 and end at total_tokens");
+    for (int b = 0; b < num_seqs; ++b) {
+      const int len = cu_seqlens_host[b + 1] - cu_seqlens_host[b];
+      if (len < 0) return fail(SLM_ERR_INVALID_ARG, "cu_seqlens decreases at %d", b);
+      if (len > max_seqlen) return fail(SLM_ERR_INVALID_ARG, "sequence %d longer than max_seqlen", b);
+    }
+  }
+  if (total_tokens == 0) return ok();
+  if (!q || !k || !v || !o || !cu_seqlens)
+    return fail(SLM_ERR_INVALID_ARG, "null q/k/v/o/cu_seqlens");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+    return fail(SLM_ERR_INVALID_ARG, "q/k/v/o must be 16-byte aligned");
+  if (o == q || o == k || o == v) return fail(SLM_ERR_INVALID_ARG, "o aliases an input");
+  const size_t need = slm_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, n_q_heads, n_kv_heads);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace ? workspace_bytes : 0, need);
+  if (!aligned16(workspace)) return fail(SLM_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+
+  const int tok = kBlockM / G;
+  const int64_t cap = prefill_tile_capacity(num_seqs, total_tokens, tok);
+  if (cap * n_kv_heads > 0x7FFFFFFF) return fail(SLM_ERR_UNSUPPORTED, "too many tiles");
+  CUtensorMap tq, tk, tv;
+  if (!encode_bf16_3d(&tq, q, head_dim, n_q_heads, total_tokens, G, tok) ||
+      !encode_bf16_3d(&tk, k, head_dim, n_kv_heads, total_tokens, 1, kBlockN) ||
+      !encode_bf16_3d(&tv, v, head_dim, n_kv_heads, total_tokens, 1, kBlockN))
+    return fail(SLM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+
+  int32_t* tiles = static_cast<int32_t*>(workspace);
+  const int max_nb = std::max(1, (max_seqlen + kBlockN - 1) / kBlockN);
+  prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, tok, max_nb, tiles,
+                                                           dev_status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "prefill schedule launch");
+
+  AttnParams p{};
+  p.n_q_heads = n_q_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.group = G;
+  p.tok_per_tile = tok;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.dev_status = dev_status;
+  p.cu_seqlens = cu_seqlens;
+  p.tiles = tiles;
+  p.total_tokens = total_tokens;
+  const int grid = static_cast<int>(cap * n_kv_heads);
+  e = (head_dim == 64) ? launch_attn<64, AttnMode::kPrefill>(tq, tk, tv, p, grid, stream)
+                       : launch_attn<128, AttnMode::kPrefill>(tq, tk, tv, p, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+  return ok();
+}
+
+slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const void* vp, const void* ks,
+                                         const void* vs, const void* k_new, const void* v_new,
+                                         const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
+                                         int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                         float softmax_scale, void* ks_out, void* vs_out, void* o, float* lse,
+                                         int32_t* dev_status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (W < 0 || Lp < 0 || L_prev < 0 || Smax < 0)
+    return fail(SLM_ERR_INVALID_ARG, "negative size (W=%d Lp=%d L_prev=%d Smax=%d)", W, Lp, L_prev, Smax);
+  if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
+    return fail(SLM_ERR_INVALID_ARG, "need n_q_heads %% n_kv_heads == 0 (got %d, %d)", n_q_heads, n_kv_heads);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(SLM_ERR_UNSUPPORTED, "head_dim %d unsupported (64 or 128)", head_dim);
+  const int G = n_q_heads / n_kv_heads;
+  if (G > kBlockM) return fail(SLM_ERR_UNSUPPORTED, "query heads per KV head %d > %d", G, kBlockM);
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
+    return fail(SLM_ERR_INVALID_ARG, "softmax_scale must be finite and > 0");
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(SLM_ERR_INVALID_ARG, "k_new and v_new: both or neither");
+  const int Ls = L_prev + (k_new ? 1 : 0);
+  if (Ls > Smax) return fail(SLM_ERR_INVALID_ARG, "suffix length %d exceeds Smax %d", Ls, Smax);
+  if (Lp + Ls < 1) return fail(SLM_ERR_INVALID_ARG, "no keys: Lp + L_s must be >= 1");
+  if (W == 0) return ok();
+  if (!q || !o) return fail(SLM_ERR_INVALID_ARG, "null q/o");
+  if (Lp > 0 && (!kp || !vp)) return fail(SLM_ERR_INVALID_ARG, "null kp/vp with Lp > 0");
+  if (L_prev > 0 && (!ks || !vs)) return fail(SLM_ERR_INVALID_ARG, "null ks/vs with L_prev > 0");
+  if (Ls > 0 && (!ks_out || !vs_out)) return fail(SLM_ERR_INVALID_ARG, "null ks_out/vs_out");
+  const void* ptrs[] = {q, kp, vp, ks, vs, k_new, v_new, ks_out, vs_out, o};
+  for (const void* ptr : ptrs)
+    if (ptr && !aligned16(ptr)) return fail(SLM_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+  if (ks_out && (ks_out == ks || ks_out == vs || vs_out == ks || vs_out == vs || ks_out == vs_out))
+    return fail(SLM_ERR_INVALID_ARG, "ks_out/vs_out must not alias ks/vs or each other");
+  if (o == q) return fail(SLM_ERR_INVALID_ARG, "o aliases q");
+
+  const int tok = kBlockM / G;
+  const int n_tiles = (W + tok - 1) / tok;
+  CUtensorMap tq, tk, tv;
+  std::memset(&tk, 0, sizeof tk);
+  std::memset(&tv, 0, sizeof tv);
+  if (!encode_bf16_3d(&tq, q, head_dim, n_q_heads, W, G, tok))
+    return fail(SLM_ERR_CUDA, "cuTensorMapEncodeTiled failed (q)");
+  if (Lp > 0 && (!encode_bf16_3d(&tk, kp, head_dim, n_kv_heads, Lp, 1, kBlockN) ||
+                 !encode_bf16_3d(&tv, vp, head_dim, n_kv_heads, Lp, 1, kBlockN)))
+    return fail(SLM_ERR_CUDA, "cuTensorMapEncodeTiled failed (prefix)");
+
+  AttnParams p{};
+  p.n_q_heads = n_q_heads;
+  p.n_kv_heads = n_kv_heads;
+  p.group = G;
+  p.tok_per_tile = tok;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.dev_status = dev_status;
+  p.ks = static_cast<const __nv_bfloat16*>(ks);
+  p.vs = static_cast<const __nv_bfloat16*>(vs);
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.parent = parent_idx;
+  p.ks_out = static_cast<__nv_bfloat16*>(ks_out);
+  p.vs_out = static_cast<__nv_bfloat16*>(vs_out);
+  p.W = W;
+  p.Lp = Lp;
+  p.L_prev = L_prev;
+  p.Smax = Smax;
+  const int grid = n_tiles * n_kv_heads;
+  cudaError_t e = (head_dim == 64) ? launch_attn<64, AttnMode::kDecodePrefix>(tq, tk, tv, p, grid, stream)
+                                   : launch_attn<128, AttnMode::kDecodePrefix>(tq, tk, tv, p, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  return ok();
+}
+
+size_t slm_beam_select_workspace_size(int32_t W_in, int32_t V, int32_t W) {
+  if (W_in <= 0 || V <= 0 || W <= 0 || static_cast<int64_t>(2) * W > V) return 0;
+  if (!beam_select_supported(W_in, V, W)) return 0;
+  return beam_select_workspace_bytes(W_in, V, W);
+}
+
+slm_status slm_beam_select(const void* logits, const float* cum_scores, int32_t W_in, int32_t V, int32_t W,
+                           int32_t* out_token, int32_t* out_parent, float* out_score, int32_t* out_cand_token,
+                           int32_t* out_cand_parent, float* out_cand_score, float* out_lse, void* workspace,
+                           size_t workspace_bytes, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (W_in <= 0 || V <= 0 || W <= 0)
+    return fail(SLM_ERR_INVALID_ARG, "sizes must be positive (W_in=%d V=%d W=%d)", W_in, V, W);
+  if (static_cast<int64_t>(2) * W > V) return fail(SLM_ERR_INVALID_ARG, "need 2W <= V (W=%d V=%d)", W, V);
+  if (!beam_select_supported(W_in, V, W))
+    return fail(SLM_ERR_UNSUPPORTED, "beam sizes W_in=%d W=%d V=%d unsupported", W_in, W, V);
+  if (!logits || !cum_scores || !out_token || !out_parent || !out_score)
+    return fail(SLM_ERR_INVALID_ARG, "null logits/cum_scores/outputs");
+  if (!aligned16(logits)) return fail(SLM_ERR_INVALID_ARG, "logits must be 16-byte aligned");
+  const size_t need = beam_select_workspace_bytes(W_in, V, W);
+  if (!workspace || workspace_bytes < need)
+    return fail(SLM_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace ? workspace_bytes : 0, need);
+  if (!aligned16(workspace)) return fail(SLM_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  cudaError_t e = launch_beam_select(logits, cum_scores, W_in, V, W, out_token, out_parent, out_score,
+                                     out_cand_token, out_cand_parent, out_cand_score, out_lse, workspace, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "beam select launch");
+  return ok();
+}
+
+slm_status slm_check_status(const int32_t* dev_status, void* stream_) {
+  if (!dev_status) return fail(SLM_ERR_INVALID_ARG, "null dev_status");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, dev_status, sizeof h, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reading dev_status");
+  if (h != 0)
+    return fail(SLM_ERR_DEVICE_CHECK, "device status 0x%x:%s%s%s", h, (h & kDevBadSeqlens) ? " bad-cu_seqlens" : "",
+                (h & kDevBadParent) ? " bad-parent-index" : "", (h & kDevPipelineTimeout) ? " pipeline-timeout" : "");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+/*
+ * slm_attn.h -- C ABI of the GB300 (sm_103a) attention hot path for bounded
+ * generation: packed variable-length causal GQA prefill, shared-prefix beam
+ * decode attention with parent-index suffix reorder, and two-stage beam
+ * candidate selection.
+ *
+ * The operations are those of the article "SLM 生成式高并发推理引擎：延迟约束下的
+ * 有效吞吐优化": section 3.1 (packed prefill), section 3.2 (request-internal
+ * shared-prefix K/V layout), section 3.3 (beam candidates and state reorder).
+ *
+ * Conventions (all entry points):
+ *   - bf16 is IEEE bfloat16; fp32 is IEEE binary32.  Dense layouts are
+ *     row-major and contiguous in the order written, e.g. [T, Hq, D].
+ *   - Every tensor pointer is DEVICE memory owned by the caller, 16-byte
+ *     aligned.  The library never allocates, frees or keeps a pointer after
+ *     the call returns.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and never synchronise, except slm_check_status.
+ *   - Arguments that can be checked on the host are; a bad one returns a
+ *     status other than SLM_OK, sets a thread-local message readable with
+ *     slm_last_error(), and enqueues nothing.  No call throws, aborts or traps.
+ *   - Conditions only the device can see (a malformed sequence boundary, an
+ *     out-of-range parent index, a stuck pipeline) make the kernel skip or
+ *     finish early and OR a bit into *dev_status (when non-NULL); the affected
+ *     outputs are then undefined.
+ *   - Query head h reads KV head h / (Hq / Hkv): contiguous head groups.
+ *   - Supported: head_dim 64 or 128; Hq % Hkv == 0; Hq / Hkv <= 128.
+ */
+#ifndef SLM_ATTN_H_
+#define SLM_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SLM_OK = 0,
+  SLM_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, aliasing, bad host boundary */
+  SLM_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels implement */
+  SLM_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (message has the CUDA error) */
+  SLM_ERR_WORKSPACE = 4,     /* workspace missing or smaller than the *_workspace_size query */
+  SLM_ERR_DEVICE_CHECK = 5   /* slm_check_status found device-side error bits */
+} slm_status;
+
+/* Device status bits (OR-ed into *dev_status by kernels). */
+#define SLM_DEV_BAD_SEQLENS 1        /* cu_seqlens not non-decreasing from 0 to total_tokens */
+#define SLM_DEV_BAD_PARENT 2         /* a parent index outside [0, W) */
+#define SLM_DEV_PIPELINE_TIMEOUT 4   /* an in-kernel bounded wait ran out (kernel ended early) */
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char* slm_last_error(void);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int32_t slm_abi_version(void);
+
+/*
+ * Packed variable-length causal GQA prefill attention (article section 3.1).
+ *
+ *   q  bf16 [T, Hq, D], k / v bf16 [T, Hkv, D]: the valid tokens of all
+ *      sequences packed back to back (no padding);
+ *   cu_seqlens int32 [num_seqs + 1] (device): sequence boundary, prefix sums
+ *      of the lengths, cu_seqlens[0] = 0, cu_seqlens[num_seqs] = T =
+ *      total_tokens; equal neighbours are allowed (empty sequences);
+ *   cu_seqlens_host (nullable): host copy of the same; when given it is
+ *      validated on the host (monotone, ends at T, lengths <= max_seqlen);
+ *   max_seqlen >= every length (sizes the schedule);
+ *   softmax_scale > 0 multiplies q.k before the softmax (1/sqrt(D) usually).
+ *
+ *   o   bf16 [T, Hq, D] (may not alias q, k, v):
+ *       o[t, h] = sum_j softmax_j(scale * q[t,h] . k[j, h/G]) v[j, h/G]
+ *       over the tokens j of t's own sequence with j <= t (block-diagonal
+ *       causal mask); fp32 accumulation and fp32 online softmax.
+ *   lse (nullable) fp32 [Hq, T]: natural-log log-sum-exp of the scaled scores.
+ *
+ *   workspace: device scratch of at least slm_prefill_workspace_size(...)
+ *   bytes (the schedule of query tiles).  dev_status: nullable device int32.
+ */
+slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                   const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens,
+                                   int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                   float softmax_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream);
+
+/* Workspace bytes slm_packed_prefill_attn needs for these sizes (0 = unsupported). */
+size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t n_q_heads,
+                                  int32_t n_kv_heads);
+
+/*
+ * Shared-prefix beam decode attention with parent-index suffix reorder
+ * (article sections 3.2 and 3.3).
+ *
+ *   q      bf16 [W, Hq, D]: one query token per beam, in the NEW beam order;
+ *   kp, vp bf16 [Lp, Hkv, D]: the prompt K/V, one copy shared by all beams
+ *          (nullable when Lp == 0);
+ *   ks, vs bf16 [W, Smax, Hkv, D]: suffix K/V of the previous step, rows
+ *          s < L_prev valid, in the PREVIOUS beam order;
+ *   k_new, v_new bf16 [W, Hkv, D] (nullable together): K/V of each beam's
+ *          new token, new order; when NULL nothing is appended;
+ *   parent_idx int32 [W] (device, nullable = identity): new beam b continues
+ *          previous beam parent_idx[b], 0 <= parent_idx[b] < W.
+ *
+ *   ks_out, vs_out bf16 [W, Smax, Hkv, D] (must not alias ks/vs): reordered
+ *          suffix, ks_out[b, s] = ks[parent_idx[b], s] for s < L_prev and
+ *          ks_out[b, L_prev] = k_new[b]; rows s >= L_s are not written.
+ *   o      bf16 [W, Hq, D]: o[b, h] = Attention(q[b, h],
+ *          [kp[:, h/G]; ks_out[b, :L_s, h/G]], [vp ...; vs_out ...]) with
+ *          L_s = L_prev + (k_new != NULL); the concatenation is never built:
+ *          prefix and suffix contributions meet in one fp32 online-softmax
+ *          state.  The prompt K/V is never reordered or copied.
+ *   lse    (nullable) fp32 [W, Hq].
+ *
+ * Requires Lp + L_s >= 1 and L_s <= Smax.
+ */
+slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const void* vp, const void* ks,
+                                         const void* vs, const void* k_new, const void* v_new,
+                                         const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
+                                         int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                         float softmax_scale, void* ks_out, void* vs_out, void* o, float* lse,
+                                         int32_t* dev_status, void* stream);
+
+/*
+ * Two-stage beam candidate selection (article section 3.3).
+ *
+ *   logits bf16 [W_in, V]: next-token logits of the W_in current beams
+ *          (W_in = 1 at the first step, else the beam width);
+ *   cum_scores fp32 [W_in]: cumulative beam scores;
+ *   W: beams to keep, 1 <= W and 2W <= V.
+ *
+ *   Per beam the 2W largest logits (ties: lower token id) give the token
+ *   ids; their scores are read from the FP32 log-softmax over the full
+ *   vocabulary, lp = fl32(x - lse_b) with lse_b the fp32 log-sum-exp of the
+ *   row, plus the beam's cumulative score, score = fl32(cum_b + lp).  The
+ *   W_in x 2W candidates are flattened and the global 2W best kept in order:
+ *   higher score first, equal scores by lower flat index (lower parent, then
+ *   the beam's own order).
+ *
+ *   out_token / out_parent int32 [W], out_score fp32 [W]: the first W (the
+ *   next beams; parent = source beam of each);
+ *   out_cand_token / out_cand_parent int32 [2W], out_cand_score fp32 [2W]
+ *   (each nullable): all 2W global candidates, for setting finished beams
+ *   aside;  out_lse (nullable) fp32 [W_in]: lse_b.
+ *
+ *   workspace: at least slm_beam_select_workspace_size(W_in, V, W) bytes.
+ */
+slm_status slm_beam_select(const void* logits, const float* cum_scores, int32_t W_in, int32_t V, int32_t W,
+                           int32_t* out_token, int32_t* out_parent, float* out_score, int32_t* out_cand_token,
+                           int32_t* out_cand_parent, float* out_cand_score, float* out_lse, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Workspace bytes slm_beam_select needs (0 = unsupported sizes). */
+size_t slm_beam_select_workspace_size(int32_t W_in, int32_t V, int32_t W);
+
+/*
+ * Test/debug helper: synchronises `stream`, reads *dev_status and returns
+ * SLM_ERR_DEVICE_CHECK (message lists the bits) if it is non-zero, else
+ * SLM_OK.  Does not clear the word.
+ */
+slm_status slm_check_status(const int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SLM_ATTN_H_ */

@@ -1,0 +1,115 @@
+"""GPU parity of slm_shared_prefix_decode_attn against the fp64 oracle.
+
+Shared-prefix beam decode (article "SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化",
+sections 3.2-3.3): every step of the two beam workloads, chained so that each
+step's reordered suffix feeds the next, plus edge cases (no prefix, a prefix
+that is not a multiple of the 128-key block, one beam, no appended row,
+identity parents, head_dim 128) and an out-of-range parent index.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_packed_varlen_gb300 import _binding as slm
+from attention_packed_varlen_gb300 import build, workloads as wl
+from tests.parity import check_attention, check_lse
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+THREADS = oracle.default_threads()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    slm.load()
+
+
+def bits(t):
+    return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True):
+    dev = torch.device(DEV)
+    W, Hq, D = d.q.shape
+    Hkv = d.kp.shape[1] if d.kp is not None else d.k_new.shape[1]
+    ks_out = torch.zeros((W, Smax, Hkv, D), dtype=torch.bfloat16, device=dev)
+    vs_out = torch.zeros_like(ks_out)
+    lse = torch.empty((W, Hq), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kp = d.kp.to(dev) if d.kp.shape[0] > 0 else None
+    vp = d.vp.to(dev) if d.vp.shape[0] > 0 else None
+    o = slm.slm_shared_prefix_decode_attn(
+        d.q.to(dev), kp, vp, ks_dev, vs_dev,
+        d.k_new.to(dev) if with_new else None, d.v_new.to(dev) if with_new else None,
+        d.parent.to(dev) if parent else None, d.L_prev, d.softmax_scale,
+        ks_out=ks_out, vs_out=vs_out, lse=lse, dev_status=status)
+    slm.slm_check_status(status)
+    return o, lse, ks_out, vs_out
+
+
+def check_step(d, ks_host, vs_host, o, lse, ks_out, vs_out, what, with_new=True, parent=True):
+    ref, ref_lse, ks_ref, vs_ref = oracle.shared_prefix_decode(
+        d.q, d.kp, d.vp, ks_host, vs_host, d.k_new if with_new else None, d.v_new if with_new else None,
+        d.parent if parent else None, d.L_prev, d.softmax_scale, n_threads=THREADS)
+    check_attention(o, ref, what)
+    check_lse(lse, ref_lse, what)
+    Ls = d.L_prev + (1 if with_new else 0)
+    np.testing.assert_array_equal(bits(ks_out)[:, :Ls], ks_ref[:, :Ls], err_msg=f"{what}: K suffix reorder")
+    np.testing.assert_array_equal(bits(vs_out)[:, :Ls], vs_ref[:, :Ls], err_msg=f"{what}: V suffix reorder")
+
+
+@pytest.mark.parametrize("workload,index", [(wl.SHORT_PROMPT_BEAM, 4), (wl.LONG_PROMPT_WIDE_BEAM, 5)])
+def test_beam_workload_all_steps_chained(workload, index):
+    W, Smax = workload.beams, workload.max_suffix
+    dev = torch.device(DEV)
+    ks_dev = vs_dev = None
+    ks_host = vs_host = None
+    for step in range(workload.steps):
+        d = wl.decode_inputs(W, workload.prefix_len, step, Smax, workload.n_q_heads, workload.n_kv_heads,
+                             workload.head_dim, seed=wl.workload_seed(index, step))
+        # the prompt K/V is the same every step: one copy per request
+        base = wl.decode_inputs(W, workload.prefix_len, 0, Smax, workload.n_q_heads, workload.n_kv_heads,
+                                workload.head_dim, seed=wl.workload_seed(index, 0))
+        d.kp, d.vp = base.kp, base.vp
+        if step == 0:
+            ks_host, vs_host = d.ks, d.vs
+            ks_dev, vs_dev = ks_host.to(dev), vs_host.to(dev)
+        o, lse, ks_out, vs_out = run_step(d, ks_dev, vs_dev, Smax)
+        check_step(d, ks_host, vs_host, o, lse, ks_out, vs_out, f"{workload.name} step {step}")
+        # the next step reads this step's reordered suffix
+        ks_dev, vs_dev = ks_out, vs_out
+        ks_host, vs_host = ks_out.cpu(), vs_out.cpu()
+
+
+@pytest.mark.parametrize("W,Lp,L_prev,Smax,hq,hkv,D,with_new,parent", [
+    (16, 0, 2, 4, 14, 2, 64, True, True),       # no prefix: suffix only
+    (16, 129, 1, 3, 14, 2, 64, True, True),     # prefix spills into a second key block
+    (1, 96, 3, 5, 14, 2, 64, True, True),       # one beam
+    (40, 64, 3, 5, 14, 2, 64, False, True),     # nothing appended
+    (40, 64, 0, 1, 14, 2, 64, True, False),     # identity parents, no history
+    (3, 200, 2, 4, 4, 2, 128, True, True),      # head_dim 128, fewer beams than a tile
+    (130, 1, 0, 2, 8, 8, 64, True, True),       # MHA, a one-token prompt, several tiles
+])
+def test_decode_edge_cases(W, Lp, L_prev, Smax, hq, hkv, D, with_new, parent):
+    d = wl.decode_inputs(W, Lp, L_prev, Smax, hq, hkv, D, seed=W + Lp + L_prev, identity_parent=not parent)
+    dev = torch.device(DEV)
+    o, lse, ks_out, vs_out = run_step(d, d.ks.to(dev), d.vs.to(dev), Smax, with_new=with_new, parent=parent)
+    check_step(d, d.ks, d.vs, o, lse, ks_out, vs_out, f"W={W} Lp={Lp} L_prev={L_prev}", with_new, parent)
+
+
+def test_decode_bad_parent_sets_device_status():
+    d = wl.decode_inputs(8, 32, 1, 3, 14, 2, 64, seed=3)
+    dev = torch.device(DEV)
+    parent = d.parent.clone()
+    parent[5] = 8                                  # == W: out of range
+    ks_out = torch.zeros((8, 3, 2, 64), dtype=torch.bfloat16, device=dev)
+    vs_out = torch.zeros_like(ks_out)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    slm.slm_shared_prefix_decode_attn(d.q.to(dev), d.kp.to(dev), d.vp.to(dev), d.ks.to(dev), d.vs.to(dev),
+                                      d.k_new.to(dev), d.v_new.to(dev), parent.to(dev), 1, d.softmax_scale,
+                                      ks_out=ks_out, vs_out=vs_out, dev_status=status)
+    with pytest.raises(slm.SlmError):
+        slm.slm_check_status(status)
+    assert int(status.item()) & 2

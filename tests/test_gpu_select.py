@@ -1,0 +1,69 @@
+"""GPU parity of slm_beam_select against the oracle's full W x V sort.
+
+Two-stage candidate selection (article "SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化",
+section 3.3) on the two beam workloads at full size (V = 151,936), the first
+step (one row), heavy ties (few distinct logits, all-equal rows), a
+vocabulary that is not a multiple of 8, 2W = V, and W = 1.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_packed_varlen_gb300 import _binding as slm
+from attention_packed_varlen_gb300 import build, workloads as wl
+from tests.parity import check_selection
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build.build()
+    slm.load()
+
+
+def run_and_check(logits, cum, W):
+    dev = torch.device(DEV)
+    res = slm.slm_beam_select(logits.to(dev), cum.to(dev), W)
+    torch.cuda.synchronize()
+    tok, par, sc, lse = oracle.beam_select(logits, cum, 2 * W)
+    near = check_selection(res, tok, par, sc, lse, logits, cum, W)
+    return res, near
+
+
+@pytest.mark.parametrize("workload,index", [(wl.SHORT_PROMPT_BEAM, 4), (wl.LONG_PROMPT_WIDE_BEAM, 5)])
+def test_beam_workload_selection(workload, index):
+    s = wl.select_inputs(workload.beams, workload.vocab, workload.beams, seed=wl.workload_seed(index, 1), step=1)
+    _, near = run_and_check(s.logits, s.cum, workload.beams)
+    assert near <= 2
+
+
+@pytest.mark.parametrize("W", [100, 400])
+def test_first_step_single_row(W):
+    s = wl.select_inputs(1, 151936, W, seed=W, step=0)
+    run_and_check(s.logits, s.cum, W)
+
+
+@pytest.mark.parametrize("W_in,V,W,levels", [(8, 1000, 8, 5), (6, 40000, 6, 3), (3, 70000, 3, 1)])
+def test_heavy_ties(W_in, V, W, levels):
+    logits = wl.quantized_logits(W_in, V, levels=levels, seed=V)
+    cum = torch.zeros(W_in, dtype=torch.float32)
+    cum[W_in // 2:] = -0.5
+    run_and_check(logits, cum, W)
+
+
+@pytest.mark.parametrize("W_in,V,W", [(5, 1001, 5), (8, 16, 8), (4, 20000, 1), (32, 50000, 32)])
+def test_odd_sizes(W_in, V, W):
+    s = wl.select_inputs(W_in, V, W, seed=V + W)
+    run_and_check(s.logits, s.cum, W)
+
+
+def test_select_repeatable():
+    s = wl.select_inputs(100, 151936, 100, seed=9)
+    dev = torch.device(DEV)
+    a = slm.slm_beam_select(s.logits.to(dev), s.cum.to(dev), 100)
+    b = slm.slm_beam_select(s.logits.to(dev), s.cum.to(dev), 100)
+    for key in a:
+        assert torch.equal(a[key], b[key]), key
