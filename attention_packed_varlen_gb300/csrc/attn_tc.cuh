@@ -328,10 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < kBlockN; c += 2) {
         const float p0 = exp2_approx(fmaf(s[c], p.scale_log2, -m_new));
         const float p1 = exp2_approx(fmaf(s[c + 1], p.scale_log2, -m_new));
-        const uint32_t pp = pack_bf16x2(p0, p1);
-        pk[c >> 1] = pp;
-        // normalise by the sum of the bf16 weights the tensor core consumes
-        lsum += __uint_as_float(pp << 16) + __uint_as_float(pp & 0xFFFF0000u);
+        lsum += p0 + p1;
+        pk[c >> 1] = pack_bf16x2(p0, p1);
       }
       l_run = l_run * alpha + lsum;
 

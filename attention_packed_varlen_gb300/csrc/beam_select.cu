@@ -7,15 +7,29 @@
 //   global 2W best (higher score first; equal scores by lower flat index,
 //   i.e. lower parent, then the beam's own candidate order) with parents.
 //
-// One kernel, one read of the logits.  CTA (c, b) streams chunk c of beam b
-// from HBM into registers (16-byte loads), computes the chunk's max and sum of
-// exp in fp32, and keeps the chunk's exact top-2W.  Pruning at chunk level is
-// safe for the same reason it is at beam level: a logit outside its chunk's
-// top 2W has at least 2W better logits in its own beam.  The last CTA of a beam
-// (an atomic ticket, no spinning) merges the chunks into the beam's FP32 log
-// normaliser and its sorted top-2W with scores; the last beam to finish picks
-// the global candidates from those sorted lists.
+// Three kernels, one read of the logits.
+//
+// 1. threshold (one CTA per beam): histograms 4096 sampled logits (64-byte
+//    runs spread over the row) by the top 12 bits of an order-preserving key
+//    and picks a candidate threshold tau_b that keeps the beam's 2W best with
+//    near certainty while passing only a few percent of the row.
+// 2. stream (CTA (c, b) = chunk c of beam b): the HBM pass.  16-byte loads
+//    into registers, chunk max on packed bf16, fp32 sum of exp2 (MUFU)
+//    against it, and a count of logits >= tau_b; one atomic per CTA reserves
+//    room in the beam's candidate buffer and the candidates are written
+//    there.  Small and spill-free so several CTAs share an SM.
+// 3. merge (one CTA per beam): FP32 log normaliser from the chunk partials,
+//    the exact top-2W of the beam's candidates (a missed threshold falls back
+//    to an exact scan of the row), sorted, with scores.  The last beam to
+//    finish (atomic ticket, no spinning) picks the global candidates from the
+//    sorted beam lists.
+//
+// Selections are radix selects whose 8-bit digits are taken relative to the
+// live key range, so clustered keys still spread over the bins of the
+// per-warp shared-memory histograms, and a select stops as soon as the bin it
+// follows holds a single key.
 #include <algorithm>
+#include <cfloat>
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -27,21 +41,25 @@ namespace sel {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxVec = 8;                       // 16-byte vectors per thread
-constexpr int kMaxChunk = kThreads * kMaxVec * 8;  // 32768 logits per CTA
-constexpr int kCap = 8192;                       // candidate slots in shared memory
+constexpr int kMaxVec = 4;                        // 16-byte vectors per thread
+constexpr int kMaxChunk = kThreads * kMaxVec * 8; // 16384 logits per stream CTA
+constexpr int kCap = 8192;                        // candidate keys per beam
+constexpr int kThrThreads = 256;                  // threshold kernel
+constexpr int kThrBins = 4096;                    // top 12 bits of the 16-bit key
+constexpr int kSampleRuns = 128;                  // runs of 32 logits sampled per beam
+constexpr int kSelCap = 2048;                     // selected keys: 2W <= 2048
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Shared {
   unsigned long long keys[kCap];
+  unsigned long long sel[kSelCap];
+  int whist[kWarps][256];
   int hist[256];
+  unsigned long long warp_u64[2][kWarps];
   int warp_i[kWarps];
   float warp_f[kWarps];
-  unsigned long long kth;
-  int k_rem;
-  int count;
-  int flag;
-  float f0;
+  unsigned long long u64;
+  int digit, k_rem, above, in_bin, counter, flag, base;
 };
 
 // ---------------------------------------------------------------------------
@@ -59,17 +77,17 @@ __device__ __forceinline__ uint32_t key_to_bf16(uint32_t key) {
   return (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
 }
 
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits) { return __uint_as_float((bits & 0xFFFFu) << 16); }
+
 __device__ __forceinline__ uint32_t f32_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (u == 0x80000000u) u = 0;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits) { return __uint_as_float((bits & 0xFFFFu) << 16); }
-
 // Beam-local candidate key: larger = earlier (higher logit, then lower id).
-__device__ __forceinline__ unsigned long long local_key(uint32_t bits, uint32_t token) {
-  return (static_cast<unsigned long long>(bf16_key(bits)) << 32) | (0xFFFFFFFFu - token);
+__device__ __forceinline__ unsigned long long local_key(uint32_t key16, uint32_t token) {
+  return (static_cast<unsigned long long>(key16) << 32) | (0xFFFFFFFFu - token);
 }
 
 // Global candidate key: higher score, then lower parent, then lower rank in
@@ -78,33 +96,47 @@ __device__ __forceinline__ unsigned long long global_key(float score, uint32_t p
   return (static_cast<unsigned long long>(f32_key(score)) << 32) | ((0xFFFFu - parent) << 16) | (0xFFFFu - rank);
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Shared memory of the stream kernel: reductions only.
+struct Small {
+  int warp_i[kWarps];
+  float warp_f[kWarps];
+  int base;
+};
+
 // ---------------------------------------------------------------------------
-// Block primitives
+// Block primitives (every thread of the CTA calls them)
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float block_max(float v, Shared& sh) {
+template <class S>
+__device__ __forceinline__ float block_max(float v, S& sh) {
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  const int w = threadIdx.x >> 5;
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.warp_f[w] = v;
+  if ((threadIdx.x & 31) == 0) sh.warp_f[threadIdx.x >> 5] = v;
   __syncthreads();
   float r = sh.warp_f[0];
   for (int i = 1; i < kWarps; ++i) r = fmaxf(r, sh.warp_f[i]);
   return r;
 }
 
-__device__ __forceinline__ float block_sum(float v, Shared& sh) {
+template <class S>
+__device__ __forceinline__ float block_sum(float v, S& sh) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5;
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.warp_f[w] = v;
+  if ((threadIdx.x & 31) == 0) sh.warp_f[threadIdx.x >> 5] = v;
   __syncthreads();
   float r = 0.f;
   for (int i = 0; i < kWarps; ++i) r += sh.warp_f[i];  // fixed order: deterministic
   return r;
 }
 
-// Exclusive prefix sum of one int per thread; returns the total through *total.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* total, Shared& sh) {
+// Exclusive prefix sum of one int per thread (thread order); *total = sum.
+template <class S>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, S& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   int x = v;
   for (int o = 1; o < 32; o <<= 1) {
@@ -123,12 +155,48 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* total, Shared& s
   return base + x - v;
 }
 
-// Warp 0 finds, from the 256-bin histogram, the bin holding the k-th largest
-// key (bins scanned from 255 down) and stores digit / remaining rank.
-__device__ __forceinline__ void pick_bin(Shared& sh, int k, int* digit_out) {
+__device__ __forceinline__ void block_minmax(unsigned long long& mn, unsigned long long& mx, Shared& sh) {
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    sh.warp_u64[0][threadIdx.x >> 5] = mn;
+    sh.warp_u64[1][threadIdx.x >> 5] = mx;
+  }
+  __syncthreads();
+  mn = ~0ull;
+  mx = 0ull;
+  for (int i = 0; i < kWarps; ++i) {
+    mn = min(mn, sh.warp_u64[0][i]);
+    mx = max(mx, sh.warp_u64[1][i]);
+  }
+}
+
+__device__ __forceinline__ void hist_clear(Shared& sh) {
+  int* h = &sh.whist[0][0];
+  for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) h[i] = 0;
+}
+
+__device__ __forceinline__ void hist_add(Shared& sh, uint32_t digit) {
+  atomicAdd(&sh.whist[threadIdx.x >> 5][digit], 1);
+}
+
+// Sums the per-warp histograms, then warp 0 finds the bin holding the k-th
+// largest item (bins walked from 255 down): digit, items above the bin, items
+// in it, and the rank left inside it.  Ends with all results visible.
+__device__ __forceinline__ void hist_pick(Shared& sh, int k) {
+  __syncthreads();
+  if (threadIdx.x < 256) {
+    int s = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += sh.whist[w][threadIdx.x];
+    sh.hist[threadIdx.x] = s;
+  }
+  __syncthreads();
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    // lane l owns bins [255 - 8l - 7, 255 - 8l], walked from the top
     int local[8];
     int s = 0;
 #pragma unroll
@@ -142,60 +210,72 @@ __device__ __forceinline__ void pick_bin(Shared& sh, int k, int* digit_out) {
       if (lane >= o) incl += y;
     }
     const int excl = incl - s;
-    const bool mine = (excl < k) && (incl >= k);
-    const unsigned ball = __ballot_sync(0xffffffffu, mine);
+    const unsigned ball = __ballot_sync(0xffffffffu, excl < k && incl >= k);
     const int owner = ball ? (__ffs(ball) - 1) : 31;
     if (lane == owner) {
-      int cum = excl, d = 255 - 8 * lane;
+      int cum = excl, d = 255 - 8 * lane, in_bin = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         if (cum + local[i] >= k) {
           d = 255 - 8 * lane - i;
+          in_bin = local[i];
           break;
         }
         cum += local[i];
       }
-      *digit_out = d;
+      sh.digit = d;
+      sh.above = cum;
+      sh.in_bin = in_bin;
       sh.k_rem = k - cum;
     }
   }
+  __syncthreads();
 }
 
-// k-th largest (1-based) of the distinct 64-bit keys produced by key_at(i),
-// i in [0, n), with the key's bits above `top_bit` all zero.  Radix select with
-// 8-bit digits from the top; only keys matching the digits fixed so far take
-// part in later passes.  Warp-aggregated histogram updates keep heavily tied
-// inputs from serialising on one counter.
-template <class KeyAt>
-__device__ unsigned long long block_kth_largest(KeyAt key_at, int n, int k, int top_bit, Shared& sh) {
-  unsigned long long prefix = 0, mask = 0;
-  int shift = ((top_bit + 1 + 7) / 8) * 8 - 8;
-  for (; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += kThreads) sh.hist[i] = 0;
+// k-th largest (1-based) of the distinct 64-bit keys every thread visits with
+// for_each(f) (f(key)).  Each pass histograms the keys still in the live range
+// [lo, hi] by the 8 bits just below the range's leading bit, then narrows the
+// range to the bin holding the k-th key; a bin with a single key ends it.
+template <class ForEach>
+__device__ unsigned long long block_kth(ForEach for_each, int k, Shared& sh) {
+  unsigned long long lo = ~0ull, hi = 0ull;
+  for_each([&](unsigned long long key) {
+    lo = min(lo, key);
+    hi = max(hi, key);
+  });
+  block_minmax(lo, hi, sh);
+  while (lo < hi) {
+    const unsigned long long span = hi - lo;
+    const int s = max(0, 64 - __clzll(span) - 8);
+    hist_clear(sh);
     __syncthreads();
-    const int n_round = (n + kThreads - 1) / kThreads * kThreads;
-    for (int i = threadIdx.x; i < n_round; i += kThreads) {
-      int digit = -1;
-      if (i < n) {
-        const unsigned long long key = key_at(i);
-        if ((key & mask) == prefix) digit = static_cast<int>((key >> shift) & 255ull);
-      }
-      const unsigned peers = __match_any_sync(0xffffffffu, digit);
-      if (digit >= 0 && (threadIdx.x & 31) == (__ffs(peers) - 1)) atomicAdd(&sh.hist[digit], __popc(peers));
-    }
-    __syncthreads();
-    int* digit_slot = &sh.count;
-    pick_bin(sh, k, digit_slot);
-    __syncthreads();
-    prefix |= static_cast<unsigned long long>(sh.count) << shift;
-    mask |= 255ull << shift;
+    const unsigned long long lo_c = lo, hi_c = hi;
+    for_each([&](unsigned long long key) {
+      if (key >= lo_c && key <= hi_c) hist_add(sh, static_cast<uint32_t>((key - lo_c) >> s));
+    });
+    hist_pick(sh, k);
+    const unsigned long long base = lo + (static_cast<unsigned long long>(sh.digit) << s);
+    const unsigned long long width = (1ull << s) - 1;
+    hi = (hi - base <= width) ? hi : base + width;
+    lo = base;
     k = sh.k_rem;
+    const int in_bin = sh.in_bin;
     __syncthreads();
+    if (in_bin == 1 && lo < hi) {
+      const unsigned long long lo_b = lo, hi_b = hi;
+      for_each([&](unsigned long long key) {
+        if (key >= lo_b && key <= hi_b) sh.u64 = key;
+      });
+      __syncthreads();
+      const unsigned long long r = sh.u64;
+      __syncthreads();
+      return r;
+    }
   }
-  return prefix;
+  return lo;
 }
 
-// Descending bitonic sort of sh.keys[0, n_pow2) (n_pow2 a power of two).
+// Descending bitonic sort of keys[0, n_pow2).
 __device__ void block_sort_desc(unsigned long long* keys, int n_pow2) {
   for (int size = 2; size <= n_pow2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -222,7 +302,7 @@ __device__ __forceinline__ int next_pow2(int x) {
 }
 
 // ---------------------------------------------------------------------------
-// The kernel
+// The kernels
 // ---------------------------------------------------------------------------
 struct Params {
   const uint16_t* logits;  // [W_in, V] bf16 bits
@@ -230,17 +310,17 @@ struct Params {
   int W_in, V, K;          // K = 2W candidates per beam and globally
   int W;
   int n_chunks, chunk;     // chunks per beam, logits per chunk (multiple of 8)
+  int sample_per;          // entries of each beam the global stage samples
   bool vec_ok;             // 16-byte loads allowed
   // workspace
-  unsigned long long* chunk_keys;  // [W_in, n_chunks, K]
-  int* chunk_count;                // [W_in, n_chunks]
+  float* tau;                      // [W_in] candidate threshold per beam
+  int* cand_count;                 // [W_in]
+  unsigned long long* cand_keys;   // [W_in, kCap]
   float* chunk_m;                  // [W_in, n_chunks]
   float* chunk_l;                  // [W_in, n_chunks]
   float* row_score;                // [W_in, K] sorted
   int* row_token;                  // [W_in, K]
-  int* row_count;                  // [W_in]
-  unsigned* tickets;               // [W_in + 1], zero at launch
-  float* row_lse;                  // [W_in]
+  unsigned* tickets;               // [W_in + 1]
   // outputs
   int32_t* out_token;
   int32_t* out_parent;
@@ -251,25 +331,158 @@ struct Params {
   float* out_lse;
 };
 
-__device__ void chunk_stage(const Params& p, Shared& sh, int b, int c);
-__device__ void beam_stage(const Params& p, Shared& sh, int b);
+// Beam b's candidate threshold from a sample of its logits; also resets the
+// beam's counter and tickets for the stream kernel that follows.
+__global__ void __launch_bounds__(kThrThreads) threshold_kernel(const Params p) {
+  __shared__ int hist[kThrBins];
+  __shared__ int warp_tot[kThrThreads / 32];
+  const int b = blockIdx.x;
+  if (threadIdx.x == 0) {
+    p.cand_count[b] = 0;
+    p.tickets[b] = 0;
+    if (b == 0) p.tickets[p.W_in] = 0;
+  }
+  const uint16_t* row = p.logits + static_cast<int64_t>(b) * p.V;
+  // A beam small enough to fit the candidate buffer keeps everything.
+  if (p.V <= kCap) {
+    if (threadIdx.x == 0) p.tau[b] = -INFINITY;
+    return;
+  }
+  for (int i = threadIdx.x; i < kThrBins; i += kThrThreads) hist[i] = 0;
+  __syncthreads();
+  // runs of 32 consecutive logits at evenly spaced starts
+  const int ns = kSampleRuns * 32;
+  const int64_t stride = (static_cast<int64_t>(p.V) - 32) / (kSampleRuns - 1);
+  for (int s = threadIdx.x; s < ns; s += kThrThreads) {
+    const int64_t idx = (s >> 5) * stride + (s & 31);
+    atomicAdd(&hist[bf16_key(row[idx]) >> 4], 1);
+  }
+  __syncthreads();
+  const float expect = static_cast<float>(p.K) * ns / p.V;
+  const int r = min(ns, static_cast<int>(ceilf(expect + 6.f * sqrtf(expect) + 8.f)));
+  // the bin holding the r-th largest sample (bins walked from the top)
+  constexpr int kPer = kThrBins / kThrThreads;  // 16 bins per thread, highest first
+  const int first = kThrBins - 1 - kPer * threadIdx.x;
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) sum += hist[first - i];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int x = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[w] = x;
+  __syncthreads();
+  int before = x - sum;
+  for (int i = 0; i < w; ++i) before += warp_tot[i];
+  if (before < r && before + sum >= r) {
+    int cum = before, bin = first;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      cum += hist[first - i];
+      if (cum >= r) {
+        bin = first - i;
+        break;
+      }
+    }
+    // lower edge of the bin: every logit of the bin passes
+    p.tau[b] = bf16_bits_to_f32(key_to_bf16(static_cast<uint32_t>(bin) << 4));
+  }
+}
+
+__device__ void beam_merge(const Params& p, Shared& sh, int b);
 __device__ void global_stage(const Params& p, Shared& sh);
 
-__global__ void __launch_bounds__(kThreads, 2) beam_select_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2) stream_kernel(const Params p) {
+  __shared__ Small sh;
+  const int c = blockIdx.x, b = blockIdx.y;
+  const int beg = c * p.chunk;
+  const int n = min(p.V - beg, p.chunk);
+  const uint16_t* src = p.logits + static_cast<int64_t>(b) * p.V + beg;
+
+  // element e of vector i of this thread sits at chunk index (i * kThreads + tid) * 8 + e
+  uint4 reg[kMaxVec];
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int idx = (i * kThreads + threadIdx.x) * 8;
+    if (p.vec_ok && idx + 8 <= n) {
+      reg[i] = __ldcs(reinterpret_cast<const uint4*>(src + idx));
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = (idx + 2 * e < n) ? src[idx + 2 * e] : 0xFF80u;  // -inf padding
+        const uint32_t hi = (idx + 2 * e + 1 < n) ? src[idx + 2 * e + 1] : 0xFF80u;
+        w[e] = lo | (hi << 16);
+      }
+      reg[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  auto word = [&](int i, int h) -> uint32_t {
+    return h == 0 ? reg[i].x : h == 1 ? reg[i].y : h == 2 ? reg[i].z : reg[i].w;
+  };
+
+  // chunk max on packed bf16 pairs (exact)
+  __nv_bfloat162 m2 = __float2bfloat162_rn(-INFINITY);
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t w = word(i, h);
+      m2 = __hmax2(m2, *reinterpret_cast<const __nv_bfloat162*>(&w));
+    }
+  const float m_c = block_max(fmaxf(__low2float(m2), __high2float(m2)), sh);
+
+  // one pass: sum of exp against the chunk max, and the candidate count
+  const float tau = p.tau[b];
+  const float mref = m_c * kLog2e;
+  float se = 0.f;
+  int cnt = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int idx = (i * kThreads + threadIdx.x) * 8;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t w = word(i, h);
+      const float x0 = __uint_as_float(w << 16), x1 = __uint_as_float(w & 0xFFFF0000u);
+      se += ex2(fmaf(x0, kLog2e, -mref)) + ex2(fmaf(x1, kLog2e, -mref));
+      cnt += (x0 >= tau && idx + 2 * h < n) + (x1 >= tau && idx + 2 * h + 1 < n);
+    }
+  }
+  const float l_c = block_sum(se, sh);
+  int total;
+  int off = block_exclusive_scan(cnt, &total, sh);
+  if (threadIdx.x == 0) sh.base = atomicAdd(&p.cand_count[b], total);
+  __syncthreads();
+  off += sh.base;
+  unsigned long long* cand = p.cand_keys + static_cast<int64_t>(b) * kCap;
+  if (cnt > 0) {
+#pragma unroll
+    for (int i = 0; i < kMaxVec; ++i) {
+      const int idx = (i * kThreads + threadIdx.x) * 8;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t w = word(i, e >> 1);
+        const uint32_t bits = (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+        if (bf16_bits_to_f32(bits) >= tau && idx + e < n) {
+          if (off < kCap) cand[off] = local_key(bf16_key(bits), static_cast<uint32_t>(beg + idx + e));
+          ++off;
+        }
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    p.chunk_m[b * p.n_chunks + c] = m_c;
+    p.chunk_l[b * p.n_chunks + c] = l_c;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) merge_kernel(const Params p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   Shared& sh = *reinterpret_cast<Shared*>(smem_raw);
-  const int c = blockIdx.x, b = blockIdx.y;
-
-  chunk_stage(p, sh, b, c);
-
-  // Ticket: the last chunk of beam b merges the beam.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) sh.flag = (atomicAdd(&p.tickets[b], 1u) == static_cast<unsigned>(p.n_chunks - 1));
-  __syncthreads();
-  if (!sh.flag) return;
-  __threadfence();
-  beam_stage(p, sh, b);
+  const int b = blockIdx.x;
+  beam_merge(p, sh, b);
 
   // Ticket: the last beam to be merged picks the global candidates.
   __threadfence();
@@ -281,297 +494,165 @@ __global__ void __launch_bounds__(kThreads, 2) beam_select_kernel(const Params p
   global_stage(p, sh);
 }
 
-// Chunk c of beam b: partial (max, sum exp) and the chunk's exact top-K.
-__device__ void chunk_stage(const Params& p, Shared& sh, int b, int c) {
-  const int beg = c * p.chunk;
-  const int n = min(p.V - beg, p.chunk);
-  const uint16_t* src = p.logits + static_cast<int64_t>(b) * p.V + beg;
-
-  // element e of vector i of this thread sits at index (i * kThreads + tid) * 8 + e
-  uint4 reg[kMaxVec];
-#pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const int idx = (i * kThreads + threadIdx.x) * 8;
-    if (p.vec_ok && idx + 8 <= n) {
-      reg[i] = __ldcs(reinterpret_cast<const uint4*>(src + idx));
-    } else {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = (idx + 2 * e < n) ? src[idx + 2 * e] : 0xFF80u;       // -inf padding
-        const uint32_t hi = (idx + 2 * e + 1 < n) ? src[idx + 2 * e + 1] : 0xFF80u;
-        w[e] = lo | (hi << 16);
-      }
-      reg[i] = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-
-  // chunk max
-  float mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&reg[i]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) mx = fmaxf(mx, fmaxf(bf16_bits_to_f32(w[e]), bf16_bits_to_f32(w[e] >> 16)));
-  }
-  const float m_c = block_max(mx, sh);
-
-  const int K = min(p.K, n);
-  // Candidate threshold from a sample (one logit per thread): a key low enough
-  // that at least K logits of the chunk are at or above it with near
-  // certainty, yet few enough to fit the candidate buffer.  If the guess
-  // misses either way, the exact path over all logits runs instead.
-  uint32_t tau = 0;  // take everything when the chunk is small
-  if (n > kCap) {
-    const int ns = min(kThreads, (n + 7) / 8);
-    const int r_s = min(ns, (2 * K * ns + n - 1) / n + 16);
-    sh.keys[threadIdx.x] = (threadIdx.x < ns) ? bf16_key(reinterpret_cast<const uint32_t*>(&reg[0])[0]) : 0ull;
-    __syncthreads();
-    const unsigned long long* sk = sh.keys;
-    tau = static_cast<uint32_t>(block_kth_largest([&](int i) { return sk[i]; }, ns, r_s, 15, sh));
-  }
-
-  // sum of exp and candidate collection in one pass
-  if (threadIdx.x == 0) sh.count = 0;
-  __syncthreads();
-  const float mref = m_c * kLog2e;
-  float se = 0.f;
-#pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const uint32_t* w = reinterpret_cast<const uint32_t*>(&reg[i]);
-    const int idx = (i * kThreads + threadIdx.x) * 8;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t bits = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-      const float x = bf16_bits_to_f32(bits);
-      se += exp2f(fmaf(x, kLog2e, -mref));
-      const bool take = (idx + e < n) && (bf16_key(bits) >= tau);
-      const unsigned ball = __ballot_sync(0xffffffffu, take);
-      if (ball) {
-        int base = 0;
-        if ((threadIdx.x & 31) == __ffs(ball) - 1) base = atomicAdd(&sh.count, __popc(ball));
-        base = __shfl_sync(0xffffffffu, base, __ffs(ball) - 1);
-        if (take) {
-          const int pos = base + __popc(ball & ((1u << (threadIdx.x & 31)) - 1u));
-          if (pos < kCap) sh.keys[pos] = local_key(bits, static_cast<uint32_t>(beg + idx + e));
-        }
-      }
-    }
-  }
-  const float l_c = block_sum(se, sh);  // contains __syncthreads
-  const int m_cand = sh.count;
-
-  unsigned long long* out = p.chunk_keys + (static_cast<int64_t>(b) * p.n_chunks + c) * p.K;
-  if (m_cand >= K && m_cand <= kCap) {
-    // exact top-K among the candidates
-    const unsigned long long* sk = sh.keys;
-    const unsigned long long kth = block_kth_largest([&](int i) { return sk[i]; }, m_cand, K, 47, sh);
-    if (threadIdx.x == 0) sh.flag = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < m_cand; i += kThreads) {
-      const unsigned long long key = sh.keys[i];
-      if (key >= kth) out[atomicAdd(&sh.flag, 1)] = key;
-    }
-  } else {
-    // exact top-K over every logit of the chunk, keys rebuilt from registers
-    auto key_at = [&](int j) -> unsigned long long {
-      // j enumerates (vector slot, element) of this thread: j = slot*8 + e
-      const int i = j >> 3, e = j & 7;
-      const int idx = (i * kThreads + threadIdx.x) * 8 + e;
-      if (idx >= n) return 0ull;  // padding: below every real key
-      const uint32_t* w = reinterpret_cast<const uint32_t*>(&reg[i]);
-      const uint32_t bits = (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu);
-      return local_key(bits, static_cast<uint32_t>(beg + idx));
-    };
-    // per-thread enumeration: each thread walks its own 64 slots; the generic
-    // selector indexes i in [0, n) over threads, so adapt: slot = i / kThreads
-    unsigned long long prefix = 0, mask = 0;
-    int k = K;
-    for (int shift = 40; shift >= 0; shift -= 8) {
-      for (int i = threadIdx.x; i < 256; i += kThreads) sh.hist[i] = 0;
-      __syncthreads();
-#pragma unroll
-      for (int j = 0; j < kMaxVec * 8; ++j) {
-        const unsigned long long key = key_at(j);
-        int digit = -1;
-        if (key != 0ull && (key & mask) == prefix) digit = static_cast<int>((key >> shift) & 255ull);
-        const unsigned peers = __match_any_sync(0xffffffffu, digit);
-        if (digit >= 0 && (threadIdx.x & 31) == (__ffs(peers) - 1)) atomicAdd(&sh.hist[digit], __popc(peers));
-      }
-      __syncthreads();
-      pick_bin(sh, k, &sh.count);
-      __syncthreads();
-      prefix |= static_cast<unsigned long long>(sh.count) << shift;
-      mask |= 255ull << shift;
-      k = sh.k_rem;
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) sh.flag = 0;
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kMaxVec * 8; ++j) {
-      const unsigned long long key = key_at(j);
-      if (key != 0ull && key >= prefix) out[atomicAdd(&sh.flag, 1)] = key;
-    }
-  }
-  if (threadIdx.x == 0) {
-    p.chunk_count[b * p.n_chunks + c] = K;
-    p.chunk_m[b * p.n_chunks + c] = m_c;
-    p.chunk_l[b * p.n_chunks + c] = l_c;
-  }
-}
-
-// Beam b: FP32 log normaliser and the sorted top-K with scores.
-__device__ void beam_stage(const Params& p, Shared& sh, int b) {
-  // log-sum-exp from the chunk partials
+// Beam b: FP32 log normaliser and the sorted top-K with scores
+// fl32(cum + fl32(x - lse)).
+__device__ void beam_merge(const Params& p, Shared& sh, int b) {
+  const int K = p.K;
   float m = -INFINITY;
   for (int c = 0; c < p.n_chunks; ++c) m = fmaxf(m, __ldcg(&p.chunk_m[b * p.n_chunks + c]));
   float l = 0.f;
   for (int c = 0; c < p.n_chunks; ++c)
-    l += __ldcg(&p.chunk_l[b * p.n_chunks + c]) * exp2f((__ldcg(&p.chunk_m[b * p.n_chunks + c]) - m) * kLog2e);
+    l += __ldcg(&p.chunk_l[b * p.n_chunks + c]) * ex2((__ldcg(&p.chunk_m[b * p.n_chunks + c]) - m) * kLog2e);
   const float lse = m + logf(l);
 
-  // gather every chunk's candidates
-  int total = 0;
-  for (int c = 0; c < p.n_chunks; ++c) {
-    const int cnt = __ldcg(&p.chunk_count[b * p.n_chunks + c]);
-    const unsigned long long* src = p.chunk_keys + (static_cast<int64_t>(b) * p.n_chunks + c) * p.K;
-    for (int i = threadIdx.x; i < cnt; i += kThreads) sh.keys[total + i] = __ldcg(&src[i]);
-    total += cnt;
+  const int c_b = __ldcg(&p.cand_count[b]);
+  if (c_b >= K && c_b <= kCap) {
+    const unsigned long long* cand = p.cand_keys + static_cast<int64_t>(b) * kCap;
+    for (int i = threadIdx.x; i < c_b; i += kThreads) sh.keys[i] = __ldcg(&cand[i]);
+    __syncthreads();
+    auto for_each_cand = [&](auto f) {
+      for (int i = threadIdx.x; i < c_b; i += kThreads) f(sh.keys[i]);
+    };
+    const unsigned long long kth = block_kth(for_each_cand, K, sh);
+    if (threadIdx.x == 0) sh.counter = 0;
+    __syncthreads();
+    for_each_cand([&](unsigned long long key) {
+      if (key >= kth) sh.sel[atomicAdd(&sh.counter, 1)] = key;
+    });
+  } else {
+    // The threshold missed (rare: a freak sample, heavy ties or -inf
+    // logits): exact top-K over the whole row.
+    const uint16_t* row = p.logits + static_cast<int64_t>(b) * p.V;
+    auto for_each_row = [&](auto f) {
+      for (int j = threadIdx.x; j < p.V; j += kThreads) f(local_key(bf16_key(row[j]), static_cast<uint32_t>(j)));
+    };
+    const unsigned long long kth = block_kth(for_each_row, K, sh);
+    if (threadIdx.x == 0) sh.counter = 0;
+    __syncthreads();
+    for_each_row([&](unsigned long long key) {
+      if (key >= kth) sh.sel[atomicAdd(&sh.counter, 1)] = key;
+    });
   }
-  __syncthreads();
-  const int K = min(p.K, total);
-  const unsigned long long* sk = sh.keys;
-  const unsigned long long kth = block_kth_largest([&](int i) { return sk[i]; }, total, K, 47, sh);
-  // compact the kept keys to the front (kept count is exactly K: keys are distinct)
-  if (threadIdx.x == 0) sh.flag = 0;
-  __syncthreads();
-  unsigned long long mine[kCap / kThreads];
-  int nm = 0;
-  for (int i = threadIdx.x; i < total; i += kThreads) {
-    const unsigned long long key = sh.keys[i];
-    if (key >= kth) mine[nm++] = key;
-  }
-  __syncthreads();
-  for (int i = 0; i < nm; ++i) sh.keys[atomicAdd(&sh.flag, 1)] = mine[i];
   const int n2 = next_pow2(K);
   __syncthreads();
-  for (int i = K + threadIdx.x; i < n2; i += kThreads) sh.keys[i] = 0ull;
-  block_sort_desc(sh.keys, n2);
+  for (int i = K + threadIdx.x; i < n2; i += kThreads) sh.sel[i] = 0ull;
+  block_sort_desc(sh.sel, n2);
 
   const float cum = p.cum[b];
   for (int r = threadIdx.x; r < K; r += kThreads) {
-    const unsigned long long key = sh.keys[r];
+    const unsigned long long key = sh.sel[r];
     const uint32_t token = 0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFull);
     const float x = bf16_bits_to_f32(key_to_bf16(static_cast<uint32_t>(key >> 32)));
-    const float lp = __fsub_rn(x, lse);      // FP32 log-probability
-    p.row_score[static_cast<int64_t>(b) * p.K + r] = __fadd_rn(cum, lp);
-    p.row_token[static_cast<int64_t>(b) * p.K + r] = static_cast<int>(token);
+    const float lp = __fsub_rn(x, lse);  // FP32 log-probability
+    p.row_score[static_cast<int64_t>(b) * K + r] = __fadd_rn(cum, lp);
+    p.row_token[static_cast<int64_t>(b) * K + r] = static_cast<int>(token);
   }
-  if (threadIdx.x == 0) {
-    p.row_count[b] = K;
-    p.row_lse[b] = lse;
-    if (p.out_lse) p.out_lse[b] = lse;
-  }
+  if (threadIdx.x == 0 && p.out_lse) p.out_lse[b] = lse;
 }
 
-// Global top-K over the W_in sorted beam lists.
+// Global top-K over the W_in sorted beam lists (each exactly K long).
 __device__ void global_stage(const Params& p, Shared& sh) {
   const int n_keep = p.K;
   const int W_in = p.W_in;
-  // 1. sample the first c entries of every beam; the n_keep-th best sample is
-  //    a lower bound of the n_keep-th best overall.
-  const int per = min(p.K, max(1, 2 * ((n_keep + W_in - 1) / W_in)));
-  const int n_s = W_in * per;  // <= kCap by construction (host checks)
-  for (int i = threadIdx.x; i < n_s; i += kThreads) {
-    const int b = i / per, r = i - b * per;
-    const int cnt = __ldcg(&p.row_count[b]);
-    sh.keys[i] = (r < cnt) ? global_key(__ldcg(&p.row_score[static_cast<int64_t>(b) * p.K + r]), b, r) : 0ull;
-  }
-  __syncthreads();
-  const unsigned long long* sk = sh.keys;
-  unsigned long long lo = block_kth_largest([&](int i) { return sk[i]; }, n_s, n_keep, 63, sh);
-
-  // 2. count entries at or above the bound, per beam (lists are sorted, so a
-  //    binary search per beam); raise the bound while they overflow.
-  auto count_at_least = [&](unsigned long long bound) -> int {
-    int local = 0;
-    for (int b = threadIdx.x; b < W_in; b += kThreads) {
-      int lo_i = 0, hi_i = __ldcg(&p.row_count[b]);  // first index with key < bound
-      while (lo_i < hi_i) {
-        const int mid = (lo_i + hi_i) >> 1;
-        const unsigned long long k = global_key(__ldcg(&p.row_score[static_cast<int64_t>(b) * p.K + mid]), b, mid);
-        if (k >= bound) lo_i = mid + 1;
-        else hi_i = mid;
-      }
-      local += lo_i;
-    }
-    int tot;
-    block_exclusive_scan(local, &tot, sh);
-    return tot;
+  const int K = p.K;
+  const int per = p.sample_per;  // W_in * per >= n_keep and <= kSelCap
+  auto gkey = [&](int b, int r) {
+    return global_key(__ldcg(&p.row_score[static_cast<int64_t>(b) * K + r]), b, r);
   };
-  int m = count_at_least(lo);
+  // 1. the first `per` entries of every beam; the n_keep-th best of them is a
+  //    lower bound of the n_keep-th best overall
+  const int n_s = W_in * per;
+  for (int i = threadIdx.x; i < n_s; i += kThreads) sh.sel[i] = gkey(i / per, i % per);
+  __syncthreads();
+  auto for_each_sample = [&](auto f) {
+    for (int i = threadIdx.x; i < n_s; i += kThreads) f(sh.sel[i]);
+  };
+  unsigned long long lo = block_kth(for_each_sample, n_keep, sh);
+
+  // 2. entries at or above the bound, per beam: from the sample, and past it
+  //    by binary search in the beam's sorted list when the whole sample clears
+  auto count_global = [&](int b, unsigned long long bound, int from) {
+    int lo_i = from, hi_i = K;
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i) >> 1;
+      if (gkey(b, mid) >= bound) lo_i = mid + 1;
+      else hi_i = mid;
+    }
+    return lo_i;
+  };
+  auto beam_count = [&](int b, unsigned long long bound) {
+    int c = 0;
+    while (c < per && sh.sel[b * per + c] >= bound) ++c;
+    if (c == per && per < K) c = count_global(b, bound, per);
+    return c;
+  };
+  constexpr int kBeamsPerThread = 2;  // W_in <= 1024
+  int cnt[kBeamsPerThread];
+  int mine = 0;
+#pragma unroll
+  for (int j = 0; j < kBeamsPerThread; ++j) {
+    const int b = threadIdx.x + j * kThreads;
+    cnt[j] = (b < W_in) ? beam_count(b, lo) : 0;
+    mine += cnt[j];
+  }
+  int m;
+  int off = block_exclusive_scan(mine, &m, sh);
   if (m > kCap) {
-    // bisect the key range: count(bound) falls by at most 1 per key value,
-    // so some bound has n_keep <= count <= kCap
+    // Rare: bisect the key range; the count drops by at most one per key
+    // value, so some bound keeps between n_keep and kCap entries.
     unsigned long long hi = ~0ull;
     while (true) {
       const unsigned long long mid = lo + (hi - lo) / 2;
-      const int cm = count_at_least(mid);
+      int part = 0;
+      for (int b = threadIdx.x; b < W_in; b += kThreads) part += count_global(b, mid, 0);
+      int cm;
+      block_exclusive_scan(part, &cm, sh);
       if (cm > kCap) lo = mid;
       else if (cm < n_keep) hi = mid;
-      else { lo = mid; m = cm; break; }
+      else {
+        lo = mid;
+        break;
+      }
     }
+    mine = 0;
+#pragma unroll
+    for (int j = 0; j < kBeamsPerThread; ++j) {
+      const int b = threadIdx.x + j * kThreads;
+      cnt[j] = (b < W_in) ? count_global(b, lo, 0) : 0;
+      mine += cnt[j];
+    }
+    off = block_exclusive_scan(mine, &m, sh);
   }
 
-  // 3. gather the entries >= lo
-  int local = 0;
-  for (int b = threadIdx.x; b < W_in; b += kThreads) {
-    int lo_i = 0, hi_i = __ldcg(&p.row_count[b]);
-    while (lo_i < hi_i) {
-      const int mid = (lo_i + hi_i) >> 1;
-      const unsigned long long k = global_key(__ldcg(&p.row_score[static_cast<int64_t>(b) * p.K + mid]), b, mid);
-      if (k >= lo) lo_i = mid + 1;
-      else hi_i = mid;
-    }
-    local += lo_i;
-  }
-  int tot;
-  int off = block_exclusive_scan(local, &tot, sh);
-  __syncthreads();
-  for (int b = threadIdx.x; b < W_in; b += kThreads) {
-    const int cnt = __ldcg(&p.row_count[b]);
-    for (int r = 0; r < cnt; ++r) {
-      const unsigned long long k = global_key(__ldcg(&p.row_score[static_cast<int64_t>(b) * p.K + r]), b, r);
-      if (k < lo) break;
-      sh.keys[off++] = k;
-    }
+  // 3. gather the entries at or above the bound
+#pragma unroll
+  for (int j = 0; j < kBeamsPerThread; ++j) {
+    const int b = threadIdx.x + j * kThreads;
+    for (int r = 0; r < cnt[j]; ++r) sh.keys[off++] = (r < per) ? sh.sel[b * per + r] : gkey(b, r);
   }
   __syncthreads();
 
   // 4. exact n_keep best, sorted
-  const unsigned long long kth = block_kth_largest([&](int i) { return sk[i]; }, tot, n_keep, 63, sh);
-  if (threadIdx.x == 0) sh.flag = 0;
+  auto for_each_m = [&](auto f) {
+    for (int i = threadIdx.x; i < m; i += kThreads) f(sh.keys[i]);
+  };
+  const unsigned long long kth = block_kth(for_each_m, n_keep, sh);
+  if (threadIdx.x == 0) sh.counter = 0;
   __syncthreads();
-  unsigned long long mine[kCap / kThreads];
-  int nm = 0;
-  for (int i = threadIdx.x; i < tot; i += kThreads) {
-    const unsigned long long key = sh.keys[i];
-    if (key >= kth) mine[nm++] = key;
-  }
-  __syncthreads();
-  for (int i = 0; i < nm; ++i) sh.keys[atomicAdd(&sh.flag, 1)] = mine[i];
+  for_each_m([&](unsigned long long key) {
+    if (key >= kth) sh.sel[atomicAdd(&sh.counter, 1)] = key;
+  });
   const int n2 = next_pow2(n_keep);
   __syncthreads();
-  for (int i = n_keep + threadIdx.x; i < n2; i += kThreads) sh.keys[i] = 0ull;
-  block_sort_desc(sh.keys, n2);
+  for (int i = n_keep + threadIdx.x; i < n2; i += kThreads) sh.sel[i] = 0ull;
+  block_sort_desc(sh.sel, n2);
 
   for (int i = threadIdx.x; i < n_keep; i += kThreads) {
-    const unsigned long long key = sh.keys[i];
+    const unsigned long long key = sh.sel[i];
     const int parent = 0xFFFF - static_cast<int>((key >> 16) & 0xFFFFull);
     const int rank = 0xFFFF - static_cast<int>(key & 0xFFFFull);
-    const int token = __ldcg(&p.row_token[static_cast<int64_t>(parent) * p.K + rank]);
-    const float score = __ldcg(&p.row_score[static_cast<int64_t>(parent) * p.K + rank]);
+    const int token = __ldcg(&p.row_token[static_cast<int64_t>(parent) * K + rank]);
+    const float score = __ldcg(&p.row_score[static_cast<int64_t>(parent) * K + rank]);
     if (i < p.W) {
       p.out_token[i] = token;
       p.out_parent[i] = parent;
@@ -591,38 +672,40 @@ __device__ void global_stage(const Params& p, Shared& sh) {
 namespace {
 
 struct SelLayout {
-  int n_chunks, chunk;
-  size_t off_keys, off_count, off_m, off_l, off_rscore, off_rtoken, off_rcount, off_tickets, off_lse, total;
+  int n_chunks, chunk, sample_per;
+  size_t off_tau, off_count, off_cand, off_m, off_l, off_rscore, off_rtoken, off_tickets, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool sel_layout(int W_in, int V, int W, SelLayout* L) {
   if (W_in <= 0 || V <= 0 || W <= 0) return false;
-  const int K = 2 * W;
-  // Chunks: at most kMaxChunk logits, enough CTAs to cover the GPU a few
-  // times over, and few enough that one beam's candidates fit the buffer.
-  int n_chunks = (V + sel::kMaxChunk - 1) / sel::kMaxChunk;
-  const int target_ctas = 1216;  // 8 per SM on 152 SMs
-  while (static_cast<int64_t>(n_chunks) * W_in < target_ctas && n_chunks * 2 * 8 <= V &&
-         (n_chunks * 2) * static_cast<int64_t>(K) <= sel::kCap)
-    n_chunks *= 2;
+  const int64_t K = 2 * static_cast<int64_t>(W);
+  if (K > sel::kSelCap || K > V || W_in > 1024 || V >= (1 << 24)) return false;
+  // Chunks: at most kMaxChunk logits, about 8 CTAs per SM over the grid
+  // (152 SMs), and at least 4096 logits each.
+  int n_chunks = std::max((V + sel::kMaxChunk - 1) / sel::kMaxChunk, (1216 + W_in / 2) / W_in);
+  n_chunks = std::min(n_chunks, std::max((V + sel::kMaxChunk - 1) / sel::kMaxChunk, V / 4096));
+  n_chunks = std::max(n_chunks, 1);
   int chunk = (V + n_chunks - 1) / n_chunks;
   chunk = (chunk + 7) / 8 * 8;
   n_chunks = (V + chunk - 1) / chunk;
-  if (static_cast<int64_t>(n_chunks) * K > sel::kCap) return false;
   L->n_chunks = n_chunks;
   L->chunk = chunk;
+  // global stage sample: as many entries per beam as fit, at least enough to
+  // hold n_keep = K entries in total
+  const int per = static_cast<int>(std::min<int64_t>(K, sel::kSelCap / W_in));
+  if (static_cast<int64_t>(per) * W_in < K) return false;
+  L->sample_per = per;
   size_t o = 0;
-  L->off_keys = o;    o = align256(o + sizeof(unsigned long long) * size_t(W_in) * n_chunks * K);
-  L->off_count = o;   o = align256(o + sizeof(int) * size_t(W_in) * n_chunks);
+  L->off_tau = o;     o = align256(o + sizeof(float) * size_t(W_in));
+  L->off_count = o;   o = align256(o + sizeof(int) * size_t(W_in));
+  L->off_cand = o;    o = align256(o + sizeof(unsigned long long) * size_t(W_in) * sel::kCap);
   L->off_m = o;       o = align256(o + sizeof(float) * size_t(W_in) * n_chunks);
   L->off_l = o;       o = align256(o + sizeof(float) * size_t(W_in) * n_chunks);
   L->off_rscore = o;  o = align256(o + sizeof(float) * size_t(W_in) * K);
   L->off_rtoken = o;  o = align256(o + sizeof(int) * size_t(W_in) * K);
-  L->off_rcount = o;  o = align256(o + sizeof(int) * size_t(W_in));
   L->off_tickets = o; o = align256(o + sizeof(unsigned) * size_t(W_in + 1));
-  L->off_lse = o;     o = align256(o + sizeof(float) * size_t(W_in));
   L->total = o;
   return true;
 }
@@ -637,11 +720,7 @@ size_t beam_select_workspace_bytes(int W_in, int V, int W) {
 
 bool beam_select_supported(int W_in, int V, int W) {
   SelLayout L;
-  if (!sel_layout(W_in, V, W, &L)) return false;
-  // the global stage samples 2 * ceil(2W / W_in) entries of every beam
-  const int K = 2 * W;
-  const int per = std::min(K, std::max(1, 2 * ((K + W_in - 1) / W_in)));
-  return static_cast<int64_t>(W_in) * per <= sel::kCap && K <= sel::kCap / 2 && W_in <= 0xFFFF && K <= 0xFFFF;
+  return sel_layout(W_in, V, W, &L);
 }
 
 cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, int V, int W, int32_t* out_token,
@@ -660,16 +739,16 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   p.W = W;
   p.n_chunks = L.n_chunks;
   p.chunk = L.chunk;
+  p.sample_per = L.sample_per;
   p.vec_ok = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
-  p.chunk_keys = reinterpret_cast<unsigned long long*>(ws + L.off_keys);
-  p.chunk_count = reinterpret_cast<int*>(ws + L.off_count);
+  p.tau = reinterpret_cast<float*>(ws + L.off_tau);
+  p.cand_count = reinterpret_cast<int*>(ws + L.off_count);
+  p.cand_keys = reinterpret_cast<unsigned long long*>(ws + L.off_cand);
   p.chunk_m = reinterpret_cast<float*>(ws + L.off_m);
   p.chunk_l = reinterpret_cast<float*>(ws + L.off_l);
   p.row_score = reinterpret_cast<float*>(ws + L.off_rscore);
   p.row_token = reinterpret_cast<int*>(ws + L.off_rtoken);
-  p.row_count = reinterpret_cast<int*>(ws + L.off_rcount);
   p.tickets = reinterpret_cast<unsigned*>(ws + L.off_tickets);
-  p.row_lse = reinterpret_cast<float*>(ws + L.off_lse);
   p.out_token = out_token;
   p.out_parent = out_parent;
   p.out_score = out_score;
@@ -678,14 +757,17 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   p.out_cand_score = out_cand_score;
   p.out_lse = out_lse;
 
-  cudaError_t e = cudaMemsetAsync(p.tickets, 0, sizeof(unsigned) * size_t(W_in + 1), stream);
+  sel::threshold_kernel<<<W_in, sel::kThrThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(sel::Shared);
-  e = cudaFuncSetAttribute(sel::beam_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
+  e = cudaFuncSetAttribute(sel::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(L.n_chunks, W_in);
-  sel::beam_select_kernel<<<grid, sel::kThreads, smem, stream>>>(p);
+  sel::stream_kernel<<<grid, sel::kThreads, 0, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  sel::merge_kernel<<<W_in, sel::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

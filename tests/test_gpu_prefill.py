@@ -70,11 +70,19 @@ def test_prefill_edge_shapes(lengths, hq, hkv, d):
 
 
 def test_prefill_large_score_range_rescales():
-    # q scaled up: scores span hundreds, so the running max jumps by more than
-    # the lazy-rescale threshold across key blocks and O is rescaled in TMEM
+    # q scaled up: scores span tens of units, so the running max jumps by more
+    # than the lazy-rescale threshold across key blocks and O is rescaled in
+    # TMEM.  The softmax is then so peaked that the bf16 rounding of P bounds
+    # the error (see tests/parity.check_attention).
     inp = wl.prefill_inputs((700, 300, 129), 16, 8, 128, seed=77)
     inp.q = (inp.q.float() * 6.0).to(torch.bfloat16)
-    full_check(inp, "large scores")
+    o, lse = run_gpu(inp)
+    cu = inp.cu_seqlens.numpy()
+    ref, ref_lse = oracle.packed_prefill(inp.q, inp.k, inp.v, cu, inp.softmax_scale, want_lse=True,
+                                         n_threads=THREADS)
+    wabs = oracle.packed_prefill(inp.q, inp.k, inp.v.abs(), cu, inp.softmax_scale, n_threads=THREADS)
+    check_attention(o, ref, "large scores", weighted_abs_v=wabs)
+    check_lse(lse, ref_lse, "large scores")
 
 
 def test_concurrent_batch_sampled_rows():
