@@ -10,7 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
-#include "attn_tc.cuh"
+#include "attn_fwd.cuh"
 #include "slm_attn.h"
 #include "slm_internal.h"
 
@@ -82,14 +82,26 @@ bool encode_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  static int cache[64] = {0};
+  if (dev < 64 && cache[dev]) return cache[dev];
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+// Persistent launch: one CTA per SM (or per unit when there are fewer).
 template <int D, AttnMode MODE>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                        int grid_x, cudaStream_t stream) {
-  auto kern = attn_tc_kernel<D, MODE>;
-  const int smem = SmemLayout<D>::kAlloc;
+                        int64_t max_units, cudaStream_t stream) {
+  auto kern = attn_fwd_kernel<D, MODE>;
+  const int smem = FwdSmem<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid_x, kThreads, smem, stream>>>(tq, tk, tv, p);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), max_units)));
+  kern<<<grid, kFwdThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -98,10 +110,13 @@ constexpr int kSchedThreads = 1024;
 constexpr int kMaxKvBlocks = 4095;  // longest sequence: 4095 * 128 tokens
 constexpr int kBuckets = 4096;
 
-// Lists the (sequence, query tile) work items, heaviest first (number of
-// 128-key blocks a tile reads, descending), after checking the boundary.
+// Lists the (sequence, pair of query tiles) work items after checking the
+// boundary: sequences by length, longest first, and inside a sequence the
+// pairs that read the most key blocks first.  Persistent CTAs take the items
+// round-robin, so the items of one sequence run at the same time on
+// different SMs and share its K/V through L2, and the short ones come last.
 __global__ void __launch_bounds__(kSchedThreads)
-    prefill_schedule_kernel(const int32_t* cu, int B, int T, int tok, int max_nb, int32_t* tiles,
+    prefill_schedule_kernel(const int32_t* cu, int B, int T, int tok2, int max_nb, int32_t* items,
                             int32_t* dev_status) {
   __shared__ int cnt[kBuckets];
   __shared__ int warp_tot[kSchedThreads / 32];
@@ -116,26 +131,25 @@ __global__ void __launch_bounds__(kSchedThreads)
   __syncthreads();
   if (bad) {
     if (threadIdx.x == 0) {
-      tiles[0] = 0;
+      items[0] = 0;
       if (dev_status) atomicOr(dev_status, kDevBadSeqlens);
     }
     return;
   }
   for (int b = threadIdx.x; b < B; b += kSchedThreads) {
     const int len = cu[b + 1] - cu[b];
-    const int nt = (len + tok - 1) / tok;
-    for (int qt = 0; qt < nt; ++qt) atomicAdd(&cnt[(min(len, (qt + 1) * tok) + kBlockN - 1) / kBlockN], 1);
+    if (len > 0) atomicAdd(&cnt[(len + kBlockN - 1) / kBlockN], (len + tok2 - 1) / tok2);
   }
   __syncthreads();
-  // exclusive scan from the heaviest bucket down: 4 buckets per thread
-  int loc[4], s = 0;
+  // exclusive scan from the longest bucket down: 4 buckets per thread
+  int loc[4], sum = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     loc[i] = cnt[kBuckets - 1 - (4 * threadIdx.x + i)];
-    s += loc[i];
+    sum += loc[i];
   }
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  int x = s;
+  int x = sum;
   for (int o = 1; o < 32; o <<= 1) {
     const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
@@ -147,7 +161,7 @@ __global__ void __launch_bounds__(kSchedThreads)
     if (i < w) base += warp_tot[i];
     total += warp_tot[i];
   }
-  int run = base + x - s;
+  int run = base + x - sum;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     cnt[kBuckets - 1 - (4 * threadIdx.x + i)] = run;
@@ -156,18 +170,20 @@ __global__ void __launch_bounds__(kSchedThreads)
   __syncthreads();
   for (int b = threadIdx.x; b < B; b += kSchedThreads) {
     const int len = cu[b + 1] - cu[b];
-    const int nt = (len + tok - 1) / tok;
-    for (int qt = 0; qt < nt; ++qt) {
-      const int pos = atomicAdd(&cnt[(min(len, (qt + 1) * tok) + kBlockN - 1) / kBlockN], 1);
-      tiles[1 + 2 * pos] = b;
-      tiles[2 + 2 * pos] = qt;
+    if (len <= 0) continue;
+    const int n_items = (len + tok2 - 1) / tok2;
+    const int pos = atomicAdd(&cnt[(len + kBlockN - 1) / kBlockN], n_items);
+    for (int k = 0; k < n_items; ++k) {
+      items[1 + 2 * (pos + k)] = b;
+      items[2 + 2 * (pos + k)] = n_items - 1 - k;
     }
   }
-  if (threadIdx.x == 0) tiles[0] = total;
+  if (threadIdx.x == 0) items[0] = total;
 }
 
-int64_t prefill_tile_capacity(int32_t num_seqs, int32_t total_tokens, int32_t tok) {
-  return static_cast<int64_t>(total_tokens) / tok + num_seqs + 1;
+// Upper bound of the work items: sum over sequences of ceil(L / (2 TOK)).
+int64_t prefill_item_capacity(int32_t num_seqs, int32_t total_tokens, int32_t tok) {
+  return static_cast<int64_t>(total_tokens) / (2 * tok) + num_seqs + 1;
 }
 
 }  // namespace
@@ -187,7 +203,7 @@ size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_
   if (num_seqs < 0 || total_tokens < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return 0;
   const int G = n_q_heads / n_kv_heads;
   if (G > kBlockM) return 0;
-  const int64_t cap = prefill_tile_capacity(num_seqs, total_tokens, kBlockM / G);
+  const int64_t cap = prefill_item_capacity(num_seqs, total_tokens, kBlockM / G);
   return static_cast<size_t>(((1 + 2 * cap) * 4 + 255) / 256 * 256);
 }
 
@@ -231,7 +247,7 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   if (!aligned16(workspace)) return fail(SLM_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
 
   const int tok = kBlockM / G;
-  const int64_t cap = prefill_tile_capacity(num_seqs, total_tokens, tok);
+  const int64_t cap = prefill_item_capacity(num_seqs, total_tokens, tok);
   if (cap * n_kv_heads > 0x7FFFFFFF) return fail(SLM_ERR_UNSUPPORTED, "too many tiles");
   CUtensorMap tq, tk, tv;
   if (!encode_bf16_3d(&tq, q, head_dim, n_q_heads, total_tokens, G, tok) ||
@@ -239,10 +255,10 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
       !encode_bf16_3d(&tv, v, head_dim, n_kv_heads, total_tokens, 1, kBlockN))
     return fail(SLM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
-  int32_t* tiles = static_cast<int32_t*>(workspace);
+  int32_t* items = static_cast<int32_t*>(workspace);
   const int max_nb = std::max(1, (max_seqlen + kBlockN - 1) / kBlockN);
-  prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, tok, max_nb, tiles,
-                                                           dev_status);
+  prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, 2 * tok, max_nb,
+                                                           items, dev_status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill schedule launch");
 
@@ -256,11 +272,10 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   p.lse = lse;
   p.dev_status = dev_status;
   p.cu_seqlens = cu_seqlens;
-  p.tiles = tiles;
+  p.items = items;
   p.total_tokens = total_tokens;
-  const int grid = static_cast<int>(cap * n_kv_heads);
-  e = (head_dim == 64) ? launch_attn<64, AttnMode::kPrefill>(tq, tk, tv, p, grid, stream)
-                       : launch_attn<128, AttnMode::kPrefill>(tq, tk, tv, p, grid, stream);
+  e = (head_dim == 64) ? launch_attn<64, AttnMode::kPrefill>(tq, tk, tv, p, cap * n_kv_heads, stream)
+                       : launch_attn<128, AttnMode::kPrefill>(tq, tk, tv, p, cap * n_kv_heads, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   return ok();
 }
@@ -299,7 +314,7 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
   if (o == q) return fail(SLM_ERR_INVALID_ARG, "o aliases q");
 
   const int tok = kBlockM / G;
-  const int n_tiles = (W + tok - 1) / tok;
+  const int64_t n_units = static_cast<int64_t>((W + 2 * tok - 1) / (2 * tok)) * n_kv_heads;
   CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof tk);
   std::memset(&tv, 0, sizeof tv);
@@ -318,6 +333,7 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.dev_status = dev_status;
+  p.q = static_cast<const __nv_bfloat16*>(q);
   p.ks = static_cast<const __nv_bfloat16*>(ks);
   p.vs = static_cast<const __nv_bfloat16*>(vs);
   p.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -329,9 +345,8 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
   p.Lp = Lp;
   p.L_prev = L_prev;
   p.Smax = Smax;
-  const int grid = n_tiles * n_kv_heads;
-  cudaError_t e = (head_dim == 64) ? launch_attn<64, AttnMode::kDecodePrefix>(tq, tk, tv, p, grid, stream)
-                                   : launch_attn<128, AttnMode::kDecodePrefix>(tq, tk, tv, p, grid, stream);
+  cudaError_t e = (head_dim == 64) ? launch_attn<64, AttnMode::kDecodePrefix>(tq, tk, tv, p, n_units, stream)
+                                   : launch_attn<128, AttnMode::kDecodePrefix>(tq, tk, tv, p, n_units, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   return ok();
 }

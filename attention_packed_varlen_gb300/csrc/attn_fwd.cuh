@@ -1,0 +1,571 @@
+// Blackwell (sm_103a) attention core shared by packed prefill and the
+// shared-prefix decode.
+//
+// A persistent CTA per SM walks a list of work units.  A unit is two query
+// sub-tiles of 128 rows that read the same keys: rows are (token, head)
+// pairs -- TOK = 128 / G consecutive tokens (prefill: positions of one
+// sequence; decode: beams) times the G query heads that share one KV head, so
+// each K/V block is loaded once for 2 x G heads ("Triton Packed GQA" in
+// section 3.1 of the article "SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化" does not
+// expand K/V heads either).
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax of sub-tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax of sub-tile 1
+//   warp  8    TMA producer: Q tiles (double-buffered across units) and a
+//              ring of K/V blocks, 128-byte swizzled
+//   warp  9    tcgen05 issuer: S_t = Q_t K^T into TMEM, then O_t += P_t V
+//              with P_t read back from TMEM where the softmax wrote it over
+//              S_t (bf16, two per column)
+//
+// Per key block the issue order is PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
+// each sub-tile's softmax overlaps the other sub-tile's MMAs.  tcgen05 work
+// completes in issue order, so a softmax that sees S_t(j+1) done also knows
+// PV_t(j) is done and may rescale O_t.  The online softmax keeps its running
+// maximum until a block raises it by more than 2^8 (the factor cancels in the
+// final division), so O is rarely rescaled.
+//
+// Every mbarrier wait is bounded (see sm103_ptx.cuh); a stuck pipeline ends
+// the kernel with a status bit instead of a hang.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "slm_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace slm {
+
+constexpr int kBlockM = 128;              // query rows per sub-tile (TMEM lanes)
+constexpr int kBlockN = 128;              // keys per block
+constexpr int kFwdThreads = 320;
+constexpr int kSubTileBytes = 128 * 128;  // 128 rows x 64 bf16, one swizzle block column
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLazyRescaleLog2 = 8.0f;
+
+enum class AttnMode : int { kPrefill = 0, kDecodePrefix = 1 };
+
+struct AttnParams {
+  int n_q_heads, n_kv_heads, group, tok_per_tile;
+  float scale_log2;          // softmax_scale * log2(e)
+  __nv_bfloat16* o;
+  float* lse;                // nullable
+  int32_t* dev_status;       // nullable
+  // prefill
+  const int32_t* cu_seqlens;
+  const int32_t* items;      // [0] = count, then (sequence, pair) items, longest sequences first
+  int total_tokens;
+  // decode
+  const __nv_bfloat16* q;    // read by the suffix merge
+  const __nv_bfloat16* ks;
+  const __nv_bfloat16* vs;
+  const __nv_bfloat16* k_new;  // nullable (no append)
+  const __nv_bfloat16* v_new;
+  const int32_t* parent;     // nullable (identity)
+  __nv_bfloat16* ks_out;
+  __nv_bfloat16* vs_out;
+  int W, Lp, L_prev, Smax;
+};
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kDSub = D / 64;
+  static constexpr int kTile = kDSub * kSubTileBytes;  // 128 rows x D bf16
+  static constexpr int kStages = (D == 128) ? 3 : 6;   // K/V ring
+  static constexpr int kQ = 0;                         // [2 buffers][2 sub-tiles]
+  static constexpr int kKV = kQ + 4 * kTile;
+  static constexpr int kBar = kKV + kStages * kTile;
+  // barrier slots
+  static constexpr int Q_FULL = 0, Q_EMPTY = 2, KV_FULL = 4, KV_EMPTY = KV_FULL + kStages,
+                       S_FULL = KV_EMPTY + kStages, P_FULL = S_FULL + 2, O_FULL = P_FULL + 2,
+                       O_EMPTY = O_FULL + 2, DRAIN = O_EMPTY + 2, kNumBars = DRAIN + 1;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 64;
+  static constexpr int kAlloc = kTotal + 1024;  // room to align the base to 1024 bytes
+};
+
+struct UnitInfo {
+  int kvh;
+  int kv_begin;   // first key row (global index into K/V)
+  int row0[2];    // first token (prefill) or beam (decode) of each sub-tile
+  int q0[2];      // prefill: position of the sub-tile's first token in its sequence
+  int n_tok[2];   // valid tokens / beams of each sub-tile
+  int nblk[2];    // key blocks each sub-tile reads
+  int nblk_max;
+};
+
+template <AttnMode MODE>
+__device__ __forceinline__ int num_units(const AttnParams& p) {
+  if constexpr (MODE == AttnMode::kPrefill) return p.items[0] * p.n_kv_heads;
+  else return ((p.W + 2 * p.tok_per_tile - 1) / (2 * p.tok_per_tile)) * p.n_kv_heads;
+}
+
+template <AttnMode MODE>
+__device__ __forceinline__ UnitInfo unit_info(const AttnParams& p, int u) {
+  UnitInfo U;
+  const int TOK = p.tok_per_tile;
+  U.kvh = u % p.n_kv_heads;
+  const int item = u / p.n_kv_heads;
+  if constexpr (MODE == AttnMode::kPrefill) {
+    const int seq = p.items[1 + 2 * item];
+    const int pair = p.items[2 + 2 * item];
+    const int s0 = p.cu_seqlens[seq];
+    const int len = p.cu_seqlens[seq + 1] - s0;
+    U.kv_begin = s0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      U.q0[t] = (2 * pair + t) * TOK;
+      U.n_tok[t] = max(0, min(TOK, len - U.q0[t]));
+      U.row0[t] = s0 + U.q0[t];
+      U.nblk[t] = U.n_tok[t] > 0 ? (U.q0[t] + U.n_tok[t] + kBlockN - 1) / kBlockN : 0;
+    }
+  } else {
+    U.kv_begin = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      U.q0[t] = 0;
+      U.row0[t] = (2 * item + t) * TOK;
+      U.n_tok[t] = max(0, min(TOK, p.W - U.row0[t]));
+      U.nblk[t] = U.n_tok[t] > 0 ? (p.Lp + kBlockN - 1) / kBlockN : 0;
+    }
+  }
+  U.nblk_max = max(U.nblk[0], U.nblk[1]);
+  return U;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int D, AttnMode MODE>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.group;
+  const int TOK = p.tok_per_tile;
+  const int rows_used = TOK * G;
+  const int n_units = num_units<MODE>(p);
+  if (static_cast<int>(blockIdx.x) >= n_units) return;
+
+  auto q_tile = [&](int qb, int t) { return smem + L::kQ + (qb * 2 + t) * L::kTile; };
+  auto kv_tile = [&](uint32_t slot) { return smem + L::kKV + slot * L::kTile; };
+
+  // ---- setup ---------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[L::Q_FULL + i], 1);
+      mbar_init(&bars[L::Q_EMPTY + i], 1);
+      mbar_init(&bars[L::S_FULL + i], 1);
+      mbar_init(&bars[L::P_FULL + i], 128);
+      mbar_init(&bars[L::O_FULL + i], 1);
+      mbar_init(&bars[L::O_EMPTY + i], 128);
+    }
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&bars[L::KV_FULL + s], 1);
+      mbar_init(&bars[L::KV_EMPTY + s], 1);
+    }
+    mbar_init(&bars[L::DRAIN], 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    if (MODE == AttnMode::kPrefill || p.Lp > 0) {  // the K/V maps are left empty when there is no prefix
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+  }
+  // Rows of the Q tiles the TMA box never covers (G not dividing 128) must
+  // hold finite values: zero them once.
+  if (rows_used < kBlockM) {
+    const int tail = kBlockM - rows_used;
+    for (int i = threadIdx.x; i < 4 * L::kDSub * tail * 8; i += kFwdThreads) {
+      const int chunk = i & 7;
+      int rest = i >> 3;
+      const int r = rows_used + rest % tail;
+      rest /= tail;
+      const int sub = rest % L::kDSub;
+      const int tile = rest / L::kDSub;
+      *reinterpret_cast<uint4*>(smem + L::kQ + tile * L::kTile + sub * kSubTileBytes + r * 128 + chunk * 16) =
+          make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 8) {
+    // ======================= TMA producer =======================
+    if (lane == 0) {
+      uint32_t kv_i = 0;
+      int it = 0;  // units with key blocks processed so far
+      bool ok = true;
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const UnitInfo U = unit_info<MODE>(p, u);
+        if (U.nblk_max == 0) continue;  // decode with an empty prefix: suffix only
+        const int qb = it & 1;
+        if (it >= 2) ok = mbar_wait(&bars[L::Q_EMPTY + qb], ((it >> 1) - 1) & 1, abort_flag);
+        if (!ok) break;
+        uint32_t q_bytes = 0;
+        for (int t = 0; t < 2; ++t)
+          if (U.n_tok[t] > 0) q_bytes += static_cast<uint32_t>(L::kDSub) * 64u * G * TOK * 2u;
+        mbar_arrive_expect_tx(&bars[L::Q_FULL + qb], q_bytes);
+        for (int t = 0; t < 2; ++t)
+          if (U.n_tok[t] > 0)
+            for (int dh = 0; dh < L::kDSub; ++dh)
+              tma_load_3d(q_tile(qb, t) + dh * kSubTileBytes, &tm_q, &bars[L::Q_FULL + qb], dh * 64, U.kvh * G,
+                          U.row0[t]);
+        for (int j = 0; j < U.nblk_max && ok; ++j) {
+          for (int kind = 0; kind < 2; ++kind) {
+            const uint32_t slot = kv_i % L::kStages, use = kv_i / L::kStages;
+            if (use >= 1) ok = mbar_wait(&bars[L::KV_EMPTY + slot], (use - 1) & 1, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars[L::KV_FULL + slot], L::kTile);
+            for (int dh = 0; dh < L::kDSub; ++dh)
+              tma_load_3d(kv_tile(slot) + dh * kSubTileBytes, kind ? &tm_v : &tm_k, &bars[L::KV_FULL + slot],
+                          dh * 64, U.kvh, U.kv_begin + j * kBlockN);
+            ++kv_i;
+          }
+        }
+        ++it;
+      }
+      if (!ok) {
+        // Let every copy already issued land before shared memory is released.
+        for (uint32_t i = kv_i > static_cast<uint32_t>(L::kStages) ? kv_i - L::kStages : 0; i < kv_i; ++i)
+          mbar_wait_drain(&bars[L::KV_FULL + i % L::kStages], (i / L::kStages) & 1);
+        for (int i = it > 2 ? it - 2 : 0; i < it; ++i) mbar_wait_drain(&bars[L::Q_FULL + (i & 1)], (i >> 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ======================= tcgen05 issuer =======================
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBlockM, kBlockN, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBlockM, D, false, true);
+      uint32_t kv_i = 0, p_cnt[2] = {0, 0}, o_used[2] = {0, 0};
+      int it = 0;
+      bool ok = true;
+      auto slot = [&](uint32_t i) { return i % L::kStages; };
+      auto phase = [&](uint32_t i) { return (i / L::kStages) & 1; };
+      auto issue_s = [&](int qb, int t, uint32_t kslot) {
+        const uint32_t qa = smem_u32(q_tile(qb, t)), ka = smem_u32(kv_tile(kslot));
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kSubTileBytes + (kk & 3) * 32;
+          umma_bf16_ss(tmem_base + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                       idesc_s, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int t, uint32_t vslot, bool accumulate) {
+        const uint32_t va = smem_u32(kv_tile(vslot));
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_bf16_ts(tmem_base + 256 + t * 128, tmem_base + t * 128 + kk * 8,
+                       sdesc_sw128(va + kk * 2048, kSubTileBytes, 1024), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+      };
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const UnitInfo U = unit_info<MODE>(p, u);
+        if (U.nblk_max == 0) continue;
+        const int qb = it & 1;
+        ok = mbar_wait(&bars[L::Q_FULL + qb], (it >> 1) & 1, abort_flag);
+        const uint32_t kbase = kv_i;
+        if (ok) ok = mbar_wait(&bars[L::KV_FULL + slot(kbase)], phase(kbase), abort_flag);
+        if (!ok) break;
+        tc_fence_after_sync();
+        for (int t = 0; t < 2; ++t)
+          if (U.nblk[t] > 0) {
+            issue_s(qb, t, slot(kbase));
+            umma_commit(&bars[L::S_FULL + t]);
+          }
+        umma_commit(&bars[L::KV_EMPTY + slot(kbase)]);
+        for (int j = 0; j < U.nblk_max && ok; ++j) {
+          const uint32_t vi = kbase + 2 * j + 1, kn = kbase + 2 * j + 2;
+          if (j + 1 < U.nblk_max) ok = mbar_wait(&bars[L::KV_FULL + slot(kn)], phase(kn), abort_flag);
+          if (ok) ok = mbar_wait(&bars[L::KV_FULL + slot(vi)], phase(vi), abort_flag);
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (j >= U.nblk[t]) continue;
+            if (j == 0 && o_used[t] > 0) ok = mbar_wait(&bars[L::O_EMPTY + t], (o_used[t] - 1) & 1, abort_flag);
+            if (ok) ok = mbar_wait(&bars[L::P_FULL + t], p_cnt[t] & 1, abort_flag);
+            if (!ok) break;
+            ++p_cnt[t];
+            tc_fence_after_sync();
+            issue_pv(t, slot(vi), j > 0);
+            if (j == U.nblk[t] - 1) {
+              umma_commit(&bars[L::O_FULL + t]);
+              ++o_used[t];
+            } else {
+              issue_s(qb, t, slot(kn));
+              umma_commit(&bars[L::S_FULL + t]);
+            }
+          }
+          if (!ok) break;
+          umma_commit(&bars[L::KV_EMPTY + slot(vi)]);
+          if (j + 1 < U.nblk_max) umma_commit(&bars[L::KV_EMPTY + slot(kn)]);
+        }
+        kv_i = kbase + 2 * U.nblk_max;
+        umma_commit(&bars[L::Q_EMPTY + qb]);
+        ++it;
+      }
+      // All MMAs issued by this thread complete before TMEM can be released.
+      umma_commit(&bars[L::DRAIN]);
+      mbar_wait_drain(&bars[L::DRAIN], 0);
+    }
+    __syncwarp();
+  } else {
+    // ======================= softmax / epilogue (two warpgroups) =======================
+    const int t = warp >> 2;              // sub-tile of this warpgroup
+    const int r = threadIdx.x & 127;      // query row == TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem_base + t * 128;
+    const uint32_t tO = tmem_base + 256 + t * 128;
+    const int t_loc = r / G;
+    const int g = r - t_loc * G;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const UnitInfo U = unit_info<MODE>(p, u);
+      if (U.n_tok[t] == 0) continue;
+      const bool row_valid = (r < rows_used) && (t_loc < U.n_tok[t]);
+      const int qpos = U.q0[t] + t_loc;
+      float m_run = -INFINITY;  // running max, log2 domain (scaled)
+      float l_run = 0.f;
+      for (int j = 0; j < U.nblk[t]; ++j) {
+        ok = warp_wait(&bars[L::S_FULL + t], s_cnt & 1, abort_flag);
+        if (!ok) break;
+        ++s_cnt;
+        tc_fence_after_sync();
+        float s[kBlockN];
+#pragma unroll
+        for (int c = 0; c < kBlockN / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld32(tS + c * 32 + lane_off, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
+        }
+        // keys past the row's reach: later than the query (prefill; this
+        // also covers keys past the sequence) or past the prefix (decode)
+        const int key0 = j * kBlockN;
+        int lim;
+        if constexpr (MODE == AttnMode::kPrefill) lim = qpos - key0;
+        else lim = p.Lp - 1 - key0;
+        if (lim < kBlockN - 1) {
+#pragma unroll
+          for (int c = 0; c < kBlockN; ++c)
+            if (c > lim) s[c] = -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
+        const float m_cand = mx * p.scale_log2;
+        float m_new = m_run;
+        if (m_cand > m_run + kLazyRescaleLog2) m_new = m_cand;
+        const float alpha = exp2_approx(m_run - m_new);  // 0 on the first block, 1 when unchanged
+        const bool rescale_o = (j > 0) && (m_new != m_run);
+        m_run = m_new;
+        float lsum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = exp2_approx(fmaf(s[h * 64 + 2 * i], p.scale_log2, -m_new));
+            const float p1 = exp2_approx(fmaf(s[h * 64 + 2 * i + 1], p.scale_log2, -m_new));
+            lsum += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(tS + h * 32 + lane_off, pk);  // P over the first half of S's columns
+        }
+        l_run = l_run * alpha + lsum;
+        // PV_t(j-1) completed before S_t(j) did, and PV_t(j) waits for P_FULL:
+        // O_t is stable here.
+        if (__any_sync(0xffffffffu, rescale_o)) {
+          const float a = rescale_o ? alpha : 1.f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t raw[32];
+            tmem_ld32(tO + c * 32 + lane_off, raw);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * a);
+            tmem_st32(tO + c * 32 + lane_off, raw);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(&bars[L::P_FULL + t]);
+      }
+      if (!ok) break;
+
+      // ---- epilogue ----
+      float acc[D];
+      if (U.nblk[t] > 0) {
+        ok = warp_wait(&bars[L::O_FULL + t], o_cnt & 1, abort_flag);
+        if (!ok) break;
+        ++o_cnt;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld32(tO + c * 32 + lane_off, raw);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[c * 32 + i] = __uint_as_float(raw[i]);
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&bars[L::O_EMPTY + t]);  // O_t may now take the next unit's products
+      } else {
+#pragma unroll
+        for (int i = 0; i < D; ++i) acc[i] = 0.f;
+      }
+      const int h = U.kvh * G + g;
+      const int rowid = U.row0[t] + t_loc;  // token (prefill) or beam (decode)
+
+      if constexpr (MODE == AttnMode::kDecodePrefix) {
+        // Suffix keys of this beam on CUDA cores: its parent's history rows
+        // then its own new row, merged into the same online-softmax state.
+        if (row_valid) {
+          int src = rowid;
+          if (p.parent) {
+            src = p.parent[rowid];
+            if (src < 0 || src >= p.W) {
+              if (p.dev_status) atomicOr(p.dev_status, kDevBadParent);
+              src = 0;
+            }
+          }
+          uint32_t q2[D / 2];  // the q row, packed bf16 pairs
+          const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(rowid) * p.n_q_heads + h) * D;
+#pragma unroll
+          for (int d = 0; d < D; d += 8) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + d));
+            q2[d / 2 + 0] = v.x;
+            q2[d / 2 + 1] = v.y;
+            q2[d / 2 + 2] = v.z;
+            q2[d / 2 + 3] = v.w;
+          }
+          const int n_suffix = p.L_prev + (p.k_new != nullptr ? 1 : 0);
+          const int64_t row_stride = static_cast<int64_t>(p.n_kv_heads) * D;
+          for (int sidx = 0; sidx < n_suffix; ++sidx) {
+            const __nv_bfloat16* krow;
+            const __nv_bfloat16* vrow;
+            if (sidx < p.L_prev) {
+              krow = p.ks + (static_cast<int64_t>(src) * p.Smax + sidx) * row_stride + U.kvh * D;
+              vrow = p.vs + (static_cast<int64_t>(src) * p.Smax + sidx) * row_stride + U.kvh * D;
+            } else {
+              krow = p.k_new + static_cast<int64_t>(rowid) * row_stride + U.kvh * D;
+              vrow = p.v_new + static_cast<int64_t>(rowid) * row_stride + U.kvh * D;
+            }
+            float dot = 0.f;
+#pragma unroll
+            for (int d = 0; d < D; d += 8) {
+              const uint4 kv = __ldg(reinterpret_cast<const uint4*>(krow + d));
+              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h2[i]);
+                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q2[d / 2 + i]));
+                dot = fmaf(qf.x, f.x, dot);
+                dot = fmaf(qf.y, f.y, dot);
+              }
+            }
+            const float sc = dot * p.scale_log2;
+            const float m_new = fmaxf(m_run, sc);
+            const float alpha = exp2_approx(m_run - m_new);
+            const float pw = exp2_approx(sc - m_new);
+            l_run = l_run * alpha + pw;
+#pragma unroll
+            for (int d = 0; d < D; d += 8) {
+              const uint4 vv = __ldg(reinterpret_cast<const uint4*>(vrow + d));
+              const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&vv);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h2[i]);
+                acc[d + 2 * i] = fmaf(acc[d + 2 * i], alpha, pw * f.x);
+                acc[d + 2 * i + 1] = fmaf(acc[d + 2 * i + 1], alpha, pw * f.y);
+              }
+            }
+            m_run = m_new;
+          }
+        }
+      }
+
+      if (row_valid) {
+        const float inv_l = 1.f / l_run;
+        const int64_t out_row = static_cast<int64_t>(rowid) * p.n_q_heads + h;
+        uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
+#pragma unroll
+        for (int d = 0; d < D; d += 8) {
+          uint4 v;
+          v.x = pack_bf16x2(acc[d + 0] * inv_l, acc[d + 1] * inv_l);
+          v.y = pack_bf16x2(acc[d + 2] * inv_l, acc[d + 3] * inv_l);
+          v.z = pack_bf16x2(acc[d + 4] * inv_l, acc[d + 5] * inv_l);
+          v.w = pack_bf16x2(acc[d + 6] * inv_l, acc[d + 7] * inv_l);
+          dst[d >> 3] = v;
+        }
+        if (p.lse) {
+          const float lse = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+          if constexpr (MODE == AttnMode::kPrefill) p.lse[static_cast<int64_t>(h) * p.total_tokens + rowid] = lse;
+          else p.lse[out_row] = lse;
+        }
+      }
+
+      if constexpr (MODE == AttnMode::kDecodePrefix) {
+        // Suffix reorder for this sub-tile's beams and KV head:
+        //   out[b, s] = in[parent[b], s] (s < L_prev), out[b, L_prev] = new[b].
+        const int n_suffix = p.L_prev + (p.k_new != nullptr ? 1 : 0);
+        const int64_t row_stride = static_cast<int64_t>(p.n_kv_heads) * D;
+        const int items = U.n_tok[t] * n_suffix * (D / 8);
+        for (int i = r; i < items; i += 128) {
+          const int chunk = i % (D / 8);
+          const int rest = i / (D / 8);
+          const int sidx = rest % n_suffix;
+          const int beam = U.row0[t] + rest / n_suffix;
+          int src = p.parent ? p.parent[beam] : beam;
+          if (src < 0 || src >= p.W) src = 0;  // flagged above
+          const int64_t dst_off = (static_cast<int64_t>(beam) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
+          uint4 kv, vv;
+          if (sidx < p.L_prev) {
+            const int64_t src_off = (static_cast<int64_t>(src) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
+            kv = __ldg(reinterpret_cast<const uint4*>(p.ks + src_off));
+            vv = __ldg(reinterpret_cast<const uint4*>(p.vs + src_off));
+          } else {
+            const int64_t src_off = static_cast<int64_t>(beam) * row_stride + U.kvh * D + chunk * 8;
+            kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src_off));
+            vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src_off));
+          }
+          *reinterpret_cast<uint4*>(p.ks_out + dst_off) = kv;
+          *reinterpret_cast<uint4*>(p.vs_out + dst_off) = vv;
+        }
+      }
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag && p.dev_status) atomicOr(p.dev_status, kDevPipelineTimeout);
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace slm
