@@ -110,7 +110,7 @@ constexpr int kSchedThreads = 1024;
 constexpr int kMaxKvBlocks = 4095;  // longest sequence: 4095 * 128 tokens
 constexpr int kBuckets = 4096;
 
-// Lists the (sequence, pair of query tiles) work items after checking the
+// Lists the (start, length, pair of query tiles) work items after checking the
 // boundary: sequences by length, longest first, and inside a sequence the
 // pairs that read the most key blocks first.  Persistent CTAs take the items
 // round-robin, so the items of one sequence run at the same time on
@@ -173,9 +173,11 @@ __global__ void __launch_bounds__(kSchedThreads)
     if (len <= 0) continue;
     const int n_items = (len + tok2 - 1) / tok2;
     const int pos = atomicAdd(&cnt[(len + kBlockN - 1) / kBlockN], n_items);
+    const int s0 = cu[b];
     for (int k = 0; k < n_items; ++k) {
-      items[1 + 2 * (pos + k)] = b;
-      items[2 + 2 * (pos + k)] = n_items - 1 - k;
+      items[1 + 3 * (pos + k)] = s0;
+      items[2 + 3 * (pos + k)] = len;
+      items[3 + 3 * (pos + k)] = n_items - 1 - k;
     }
   }
   if (threadIdx.x == 0) items[0] = total;
@@ -204,7 +206,7 @@ size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_
   const int G = n_q_heads / n_kv_heads;
   if (G > kBlockM) return 0;
   const int64_t cap = prefill_item_capacity(num_seqs, total_tokens, kBlockM / G);
-  return static_cast<size_t>(((1 + 2 * cap) * 4 + 255) / 256 * 256);
+  return static_cast<size_t>(((1 + 3 * cap) * 4 + 255) / 256 * 256);
 }
 
 slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,

@@ -12,8 +12,8 @@
 // Warp roles (320 threads):
 //   warps 0-3  softmax of sub-tile 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax of sub-tile 1
-//   warp  8    TMA producer: Q tiles (double-buffered across units) and a
-//              ring of K/V blocks, 128-byte swizzled
+//   warp  8    TMA producer: lane 1 loads Q tiles (double-buffered across
+//              units), lane 0 a ring of K/V blocks, 128-byte swizzled
 //   warp  9    tcgen05 issuer: S_t = Q_t K^T into TMEM, then O_t += P_t V
 //              with P_t read back from TMEM where the softmax wrote it over
 //              S_t (bf16, two per column)
@@ -55,7 +55,7 @@ struct AttnParams {
   int32_t* dev_status;       // nullable
   // prefill
   const int32_t* cu_seqlens;
-  const int32_t* items;      // [0] = count, then (sequence, pair) items, longest sequences first
+  const int32_t* items;      // [0] = count, then (start, length, pair) per item, longest sequences first
   int total_tokens;
   // decode
   const __nv_bfloat16* q;    // read by the suffix merge
@@ -102,17 +102,35 @@ __device__ __forceinline__ int num_units(const AttnParams& p) {
   else return ((p.W + 2 * p.tok_per_tile - 1) / (2 * p.tok_per_tile)) * p.n_kv_heads;
 }
 
+// The memory part of a unit's description: the (start, length, pair) item
+// of prefill.  Loaded a whole unit ahead and only combined when needed, so
+// the load latency hides behind the current unit.
+struct UnitRaw {
+  int s0, len, pair;
+};
+
 template <AttnMode MODE>
-__device__ __forceinline__ UnitInfo unit_info(const AttnParams& p, int u) {
+__device__ __forceinline__ UnitRaw unit_raw(const AttnParams& p, int u) {
+  UnitRaw r{0, 0, 0};
+  if constexpr (MODE == AttnMode::kPrefill) {
+    const int item = u / p.n_kv_heads;
+    r.s0 = __ldg(&p.items[1 + 3 * item]);
+    r.len = __ldg(&p.items[2 + 3 * item]);
+    r.pair = __ldg(&p.items[3 + 3 * item]);
+  }
+  return r;
+}
+
+template <AttnMode MODE>
+__device__ __forceinline__ UnitInfo unit_info(const AttnParams& p, int u, const UnitRaw& raw) {
   UnitInfo U;
   const int TOK = p.tok_per_tile;
   U.kvh = u % p.n_kv_heads;
   const int item = u / p.n_kv_heads;
   if constexpr (MODE == AttnMode::kPrefill) {
-    const int seq = p.items[1 + 2 * item];
-    const int pair = p.items[2 + 2 * item];
-    const int s0 = p.cu_seqlens[seq];
-    const int len = p.cu_seqlens[seq + 1] - s0;
+    const int s0 = raw.s0;
+    const int len = raw.len;
+    const int pair = raw.pair;
     U.kv_begin = s0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -214,15 +232,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   if (warp == 8) {
     // ======================= TMA producer =======================
-    if (lane == 0) {
-      uint32_t kv_i = 0;
-      int it = 0;  // units with key blocks processed so far
+    // Two lanes, each blocking only on its own resource (independent thread
+    // scheduling lets them progress separately): lane 1 streams the Q tiles
+    // into the two Q buffers, as far ahead as the buffers allow; lane 0
+    // streams K/V blocks through the ring.
+    if (lane == 1) {
+      int qi = 0;
       bool ok = true;
+      UnitRaw rn = unit_raw<MODE>(p, blockIdx.x);
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const UnitInfo U = unit_info<MODE>(p, u);
+        const UnitInfo U = unit_info<MODE>(p, u, rn);
+        if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
         if (U.nblk_max == 0) continue;  // decode with an empty prefix: suffix only
-        const int qb = it & 1;
-        if (it >= 2) ok = mbar_wait(&bars[L::Q_EMPTY + qb], ((it >> 1) - 1) & 1, abort_flag);
+        const int qb = qi & 1;
+        if (qi >= 2) ok = mbar_wait(&bars[L::Q_EMPTY + qb], ((qi >> 1) - 1) & 1, abort_flag);
         if (!ok) break;
         uint32_t q_bytes = 0;
         for (int t = 0; t < 2; ++t)
@@ -233,6 +256,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int dh = 0; dh < L::kDSub; ++dh)
               tma_load_3d(q_tile(qb, t) + dh * kSubTileBytes, &tm_q, &bars[L::Q_FULL + qb], dh * 64, U.kvh * G,
                           U.row0[t]);
+        ++qi;
+      }
+      if (!ok)  // let the copies already issued land before shared memory is released
+        for (int i = qi > 2 ? qi - 2 : 0; i < qi; ++i) mbar_wait_drain(&bars[L::Q_FULL + (i & 1)], (i >> 1) & 1);
+    } else if (lane == 0) {
+      uint32_t kv_i = 0;
+      bool ok = true;
+      UnitRaw rn = unit_raw<MODE>(p, blockIdx.x);
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const UnitInfo U = unit_info<MODE>(p, u, rn);
+        if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
         for (int j = 0; j < U.nblk_max && ok; ++j) {
           for (int kind = 0; kind < 2; ++kind) {
             const uint32_t slot = kv_i % L::kStages, use = kv_i / L::kStages;
@@ -245,14 +279,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             ++kv_i;
           }
         }
-        ++it;
       }
-      if (!ok) {
-        // Let every copy already issued land before shared memory is released.
+      if (!ok)
         for (uint32_t i = kv_i > static_cast<uint32_t>(L::kStages) ? kv_i - L::kStages : 0; i < kv_i; ++i)
           mbar_wait_drain(&bars[L::KV_FULL + i % L::kStages], (i / L::kStages) & 1);
-        for (int i = it > 2 ? it - 2 : 0; i < it; ++i) mbar_wait_drain(&bars[L::Q_FULL + (i & 1)], (i >> 1) & 1);
-      }
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -281,8 +311,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           umma_bf16_ts(tmem_base + 256 + t * 128, tmem_base + t * 128 + kk * 8,
                        sdesc_sw128(va + kk * 2048, kSubTileBytes, 1024), idesc_o, (accumulate || kk > 0) ? 1u : 0u);
       };
+      UnitRaw rn = unit_raw<MODE>(p, blockIdx.x);
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const UnitInfo U = unit_info<MODE>(p, u);
+        const UnitInfo U = unit_info<MODE>(p, u, rn);
+        // the next unit's item loads while this one runs
+        if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
         if (U.nblk_max == 0) continue;
         const int qb = it & 1;
         ok = mbar_wait(&bars[L::Q_FULL + qb], (it >> 1) & 1, abort_flag);
@@ -298,8 +331,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         umma_commit(&bars[L::KV_EMPTY + slot(kbase)]);
         for (int j = 0; j < U.nblk_max && ok; ++j) {
           const uint32_t vi = kbase + 2 * j + 1, kn = kbase + 2 * j + 2;
-          if (j + 1 < U.nblk_max) ok = mbar_wait(&bars[L::KV_FULL + slot(kn)], phase(kn), abort_flag);
-          if (ok) ok = mbar_wait(&bars[L::KV_FULL + slot(vi)], phase(vi), abort_flag);
+          ok = mbar_wait(&bars[L::KV_FULL + slot(vi)], phase(vi), abort_flag);
+          bool k_next_ready = false;  // K_{j+1} is waited for only by the S that needs it
           for (int t = 0; t < 2 && ok; ++t) {
             if (j >= U.nblk[t]) continue;
             if (j == 0 && o_used[t] > 0) ok = mbar_wait(&bars[L::O_EMPTY + t], (o_used[t] - 1) & 1, abort_flag);
@@ -312,6 +345,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               umma_commit(&bars[L::O_FULL + t]);
               ++o_used[t];
             } else {
+              if (!k_next_ready) {
+                ok = mbar_wait(&bars[L::KV_FULL + slot(kn)], phase(kn), abort_flag);
+                if (!ok) break;
+                tc_fence_after_sync();
+                k_next_ready = true;
+              }
               issue_s(qb, t, slot(kn));
               umma_commit(&bars[L::S_FULL + t]);
             }
@@ -340,8 +379,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int g = r - t_loc * G;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
+    UnitRaw rn = unit_raw<MODE>(p, blockIdx.x);
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const UnitInfo U = unit_info<MODE>(p, u);
+      const UnitInfo U = unit_info<MODE>(p, u, rn);
+      if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
       if (U.n_tok[t] == 0) continue;
       const bool row_valid = (r < rows_used) && (t_loc < U.n_tok[t]);
       const int qpos = U.q0[t] + t_loc;
@@ -353,13 +394,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++s_cnt;
         tc_fence_after_sync();
         float s[kBlockN];
+        {
+          uint32_t raw[kBlockN];
 #pragma unroll
-        for (int c = 0; c < kBlockN / 32; ++c) {
-          uint32_t raw[32];
-          tmem_ld32(tS + c * 32 + lane_off, raw);
+          for (int c = 0; c < kBlockN / 32; ++c)
+            tmem_ld32(tS + c * 32 + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(raw[i]);
+          for (int i = 0; i < kBlockN; ++i) s[i] = __uint_as_float(raw[i]);
         }
         // keys past the row's reach: later than the query (prefill; this
         // also covers keys past the sequence) or past the prefix (decode)
@@ -372,16 +414,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int c = 0; c < kBlockN; ++c)
             if (c > lim) s[c] = -INFINITY;
         }
-        float mx = -INFINITY;
+        float mx8[8];  // eight independent max chains
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
+        for (int i = 0; i < 8; ++i) mx8[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < kBlockN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s[c]);
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float m_cand = mx * p.scale_log2;
         float m_new = m_run;
         if (m_cand > m_run + kLazyRescaleLog2) m_new = m_cand;
         const float alpha = exp2_approx(m_run - m_new);  // 0 on the first block, 1 when unchanged
         const bool rescale_o = (j > 0) && (m_new != m_run);
         m_run = m_new;
-        float lsum = 0.f;
+        float ls4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent sum chains
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
@@ -389,12 +435,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int i = 0; i < 32; ++i) {
             const float p0 = exp2_approx(fmaf(s[h * 64 + 2 * i], p.scale_log2, -m_new));
             const float p1 = exp2_approx(fmaf(s[h * 64 + 2 * i + 1], p.scale_log2, -m_new));
-            lsum += p0 + p1;
+            ls4[i & 3] += p0 + p1;
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st32(tS + h * 32 + lane_off, pk);  // P over the first half of S's columns
         }
-        l_run = l_run * alpha + lsum;
+        l_run = l_run * alpha + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
         // PV_t(j-1) completed before S_t(j) did, and PV_t(j) waits for P_FULL:
         // O_t is stable here.
         if (__any_sync(0xffffffffu, rescale_o)) {

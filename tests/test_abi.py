@@ -44,11 +44,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_workspace_size_queries(lib):
-    # one int32 count plus (sequence, pair of 64-token tiles) items, rounded
-    # to 256 bytes
+    # one int32 count plus (start, length, pair of 64-token tiles) items,
+    # rounded to 256 bytes
     n = _binding.slm_prefill_workspace_size(240, 130560, 1024, 16, 8)
     assert n > 0 and n % 256 == 0
-    assert n >= 4 * (1 + 2 * (130560 // 128 + 240))
+    assert n >= 4 * (1 + 3 * (130560 // 128 + 240))
     assert _binding.slm_prefill_workspace_size(4, 320, 128, 4, 3) == 0      # Hq % Hkv != 0
     assert _binding.slm_beam_select_workspace_size(100, 151936, 100) > 0
     assert _binding.slm_beam_select_workspace_size(400, 151936, 400) > 0
