@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "SLM_OK", 1: "SLM_ERR_INVALID_ARG", 2: "SLM_ERR_UNSUPPORTED",
 
 EXPORTS = ("slm_last_error", "slm_abi_version", "slm_packed_prefill_attn", "slm_prefill_workspace_size",
            "slm_shared_prefix_decode_attn", "slm_beam_select", "slm_beam_select_workspace_size",
-           "slm_check_status")
+           "slm_check_status", "slm_packed_prefill_attn_noalloc")
 
 
 class SlmError(RuntimeError):
@@ -66,6 +66,8 @@ def load(path: Optional[str] = None):
         lib.slm_beam_select_workspace_size.argtypes = [i32, i32, i32]
         lib.slm_check_status.restype = ctypes.c_int
         lib.slm_check_status.argtypes = [P, P]
+        lib.slm_packed_prefill_attn_noalloc.restype = ctypes.c_int
+        lib.slm_packed_prefill_attn_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
         if path is None:
             _lib = lib
         return lib

@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include <cuda.h>
@@ -396,3 +397,74 @@ slm_status slm_check_status(const int32_t* dev_status, void* stream_) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Prefill without a caller workspace.
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: code inside a frozen, ahead-of-time compiled graph whose memory
+// plan is fixed, a runtime whose only allocator is busy or forbidden on the
+// hot path, or a plugin host that hands out inputs and outputs but no scratch.
+// For them the tile schedule lives in a fixed array of this library's own
+// device memory, created when the library is loaded on a GPU and held until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Work items the array holds: one int32 count plus (start, length, pair)
+// per item, 192 KiB in total.
+constexpr int64_t kNoAllocMaxItems = 16383;
+constexpr int64_t kNoAllocInts = 1 + 3 * kNoAllocMaxItems + 2;  // padded to 256-byte multiple
+static __device__ __align__(256) int32_t g_noalloc_items[kNoAllocInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[kMaxDevices] = {nullptr};
+
+// Device address of the array on the current device, looked up once per
+// device (host code only ever sees a stand-in for the symbol).
+slm_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(SLM_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_items);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in prefill schedule buffer");
+    g_noalloc_addr[dev] = ptr;
+  }
+  *out = g_noalloc_addr[dev];
+  return SLM_OK;
+}
+
+}  // namespace
+
+extern "C" slm_status slm_packed_prefill_attn_noalloc(const void* q, const void* k, const void* v,
+                                                       const int32_t* cu_seqlens, const int32_t* cu_seqlens_host,
+                                                       int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen,
+                                                       int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                                       float softmax_scale, void* o, float* lse, int32_t* dev_status,
+                                                       void* stream) {
+  if (num_seqs < 0 || total_tokens < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
+    return slm_packed_prefill_attn(q, k, v, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens, max_seqlen,
+                                   n_q_heads, n_kv_heads, head_dim, softmax_scale, o, lse, nullptr, 0, dev_status,
+                                   stream);  // reports the argument error
+  const int G = n_q_heads / n_kv_heads;
+  if (G <= kBlockM) {
+    const int64_t items = prefill_item_capacity(num_seqs, total_tokens, kBlockM / G);
+    if (items > kNoAllocMaxItems)
+      return fail(SLM_ERR_UNSUPPORTED,
+                  "slm_packed_prefill_attn_noalloc: %lld work items exceed its built-in buffer of %lld "
+                  "(items = total_tokens / (2 * (128 / (n_q_heads / n_kv_heads))) + num_seqs + 1); "
+                  "use slm_packed_prefill_attn with a workspace",
+                  static_cast<long long>(items), static_cast<long long>(kNoAllocMaxItems));
+  }
+  void* scratch = nullptr;
+  const slm_status st = noalloc_scratch(&scratch);
+  if (st != SLM_OK) return st;
+  return slm_packed_prefill_attn(q, k, v, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens, max_seqlen, n_q_heads,
+                                 n_kv_heads, head_dim, softmax_scale, o, lse, scratch, sizeof(g_noalloc_items),
+                                 dev_status, stream);
+}

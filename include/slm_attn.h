@@ -154,6 +154,33 @@ slm_status slm_beam_select(const void* logits, const float* cum_scores, int32_t 
 size_t slm_beam_select_workspace_size(int32_t W_in, int32_t V, int32_t W);
 
 /*
+ * slm_packed_prefill_attn without a workspace argument.  The article has no
+ * counterpart; this entry point exists for callers that cannot allocate
+ * device memory where they run attention (a frozen ahead-of-time compiled
+ * graph with a fixed memory plan, a host that owns all allocation, a hot path
+ * on which allocation is forbidden).
+ *
+ * Arguments and results are those of slm_packed_prefill_attn.  The tile
+ * schedule is kept in a 192 KiB array of this library's own device memory
+ * that every GPU which loads the library holds until the process exits.
+ *   - Limit: total_tokens / (2 * (128 / (n_q_heads / n_kv_heads))) +
+ *     num_seqs + 1 <= 16383 work items (e.g. 130,000 tokens in 240 sequences
+ *     with 16 query / 8 KV heads use about 1,260); larger requests return
+ *     SLM_ERR_UNSUPPORTED and enqueue nothing.
+ *   - The first call on each device looks up the array's device address (no
+ *     allocation); make that first call before any stream capture.
+ *   - All calls share the one array and each overwrites it: calls that can
+ *     overlap on the GPU (different streams without ordering) race and give
+ *     wrong results.  Nothing needs clearing between calls.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+slm_status slm_packed_prefill_attn_noalloc(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                           const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens,
+                                           int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads,
+                                           int32_t head_dim, float softmax_scale, void* o, float* lse,
+                                           int32_t* dev_status, void* stream);
+
+/*
  * Test/debug helper: synchronises `stream`, reads *dev_status and returns
  * SLM_ERR_DEVICE_CHECK (message lists the bits) if it is non-zero, else
  * SLM_OK.  Does not clear the word.
