@@ -81,6 +81,8 @@ def load_peaks():
 # Clock sampling during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
+    """nvidia-smi sampling every 50 ms on a reader thread; summary() keeps the
+    samples taken between mark_start() and mark_end() (the timed region)."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -88,32 +90,57 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu_index = gpu_index
         self.proc = None
-        self.out = None
+        self.lines = []  # (host time, line)
+        self.t0 = self.t1 = None
+        self.thread = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        deadline = time.perf_counter() + 5.0  # sampling must be running before the timed region
+        while not self.lines and time.perf_counter() < deadline:
+            time.sleep(0.01)
         return self
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(0.06)
             self.proc.terminate()
             try:
-                self.out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out, _ = self.proc.communicate()
+            if self.thread is not None:
+                self.thread.join(timeout=5)
 
     def summary(self):
-        if not self.out:
+        if not self.lines:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["clock sampling unavailable"]}
+        t0 = self.t0 if self.t0 is not None else -1e30
+        t1 = (self.t1 if self.t1 is not None else 1e30) + 0.05
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -126,9 +153,26 @@ class ClockSampler:
                 if val.lower() == "active":
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock sample inside the timed region"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+# DRAM bytes (read + write) per prefill launch on this workload, from an ncu
+# capture of `bench.py --ncu-case prefill` (one layer of the same batch), keyed
+# by the kernel source it was taken on; any other source reports null.
+PREFILL_TRAFFIC = {"2f8683730f323e49": 1.166724e9 + 0.502974e9}
+
+
+def prefill_traffic():
+    import hashlib
+    path = os.path.join(ROOT, "attention_packed_varlen_gb300", "csrc", "attn_fwd.cuh")
+    try:
+        with open(path, "rb") as f:
+            key = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return PREFILL_TRAFFIC.get(key)
 
 
 # ----------------------------------------------------------------------------
@@ -356,11 +400,13 @@ def run_gpu(args):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.mark_start()
         t_start.record(stream)
         for k in range(args.steps):
             one_step(recs[k])
         t_end.record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -430,7 +476,8 @@ def run_gpu(args):
         tfl, cores, desc = oracle_prefill_sample(budget_s=args.ref_budget)
         cpu = {"value": tfl, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "cpu": cpu_model()}
 
-    launches_per_step = n_pre * 2 + sum(n_dec) * 2
+    # prefill: schedule + attention; decode step: attention + 3 selection kernels
+    launches_per_step = n_pre * 2 + sum(n_dec) * 4
     peak_sust = peaks["bf16_tflops_sustained"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -448,7 +495,7 @@ def run_gpu(args):
         "roofline": {"kernel": "slm_packed_prefill_attn (schedule + tcgen05 attention)", "bound": "tensor",
                      "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s", "frac": achieved / peak_sust,
                      "peak_kind": f"bf16 sustained, {peaks['source']}",
-                     "hbm_achieved_gbs": ps.bytes / avg_launch_s / 1e9, "traffic": args.traffic},
+                     "hbm_achieved_gbs": ps.bytes / avg_launch_s / 1e9, "traffic": args.traffic if args.traffic is not None else prefill_traffic()},
         "clocks": clk.summary(),
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
