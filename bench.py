@@ -328,6 +328,31 @@ def dist_setup(args):
     return rank, world, local
 
 
+def rank_prefill_seed(rank: int) -> int:
+    """Each rank draws its own independent batch of the same workload (weak
+    scaling: the units are whole requests, nothing is exchanged)."""
+    return PREFILL_SEED + 7919 * rank
+
+
+def rank_beam_seed(bw, rank: int) -> int:
+    return wl.workload_seed(5 if bw is wl.LONG_PROMPT_WIDE_BEAM else 4) + rank
+
+
+def max_over_ranks_of(x: float, world: int, dev) -> float:
+    """The slowest rank's time: the job is done when every rank is."""
+    if world == 1:
+        return x
+    tt = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(units_per_rank: float, world: int, slowest_s: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest
+    rank's time."""
+    return units_per_rank * world / slowest_s
+
+
 def run_reference(args):
     rank, world, _ = dist_setup(args)
     if rank != 0:
@@ -360,11 +385,10 @@ def run_gpu(args):
     from attention_packed_varlen_gb300 import _binding as slm
     lib = slm.load()
     peaks = load_peaks()
-    seed = PREFILL_SEED + 7919 * rank  # each rank: its own independent batch (weak scaling)
+    seed = rank_prefill_seed(rank)
 
     ps = PrefillSet(dev, PREFILL_WL.layers, seed)
-    beams = [BeamSet(dev, bw, wl.workload_seed(5 if bw is wl.LONG_PROMPT_WIDE_BEAM else 4) + rank)
-             for bw in BEAM_WLS]
+    beams = [BeamSet(dev, bw, rank_beam_seed(bw, rank)) for bw in BEAM_WLS]
     torch.cuda.synchronize()
 
     stream = torch.cuda.current_stream(dev)
@@ -414,25 +438,17 @@ def run_gpu(args):
     dec_ms = [[[r["dec"][j][t][0].elapsed_time(r["dec"][j][t][1]) for t in range(n_dec[j])] for r in recs]
               for j in range(len(beams))]
 
-    # max over ranks
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        tt = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        return float(tt.item())
-
+    max_over_ranks = lambda x: max_over_ranks_of(x, world, dev)
     prefill_time_s = max_over_ranks(sum(pre_ms) / 1e3)
     total_ms = max_over_ranks(total_ms)
-    flops_all = ps.flops * n_pre * args.steps * world
-    value = flops_all / prefill_time_s / 1e12
+    value = job_throughput(ps.flops * n_pre * args.steps, world, prefill_time_s) / 1e12
     avg_launch_s = sum(pre_ms) / len(pre_ms) / 1e3
     achieved = ps.flops / avg_launch_s / 1e12
 
     decode = {}
     for j, bs in enumerate(beams):
         bw = bs.w
-        per_step_us = float(np.mean(dec_ms[j])) * 1e3
+        per_step_us = max_over_ranks(float(np.mean(dec_ms[j]))) * 1e3
         bytes_step = np.mean([decode_attn_bytes(bw.beams, bw.prefix_len, t, bw.n_q_heads, bw.n_kv_heads,
                                                 bw.head_dim) for t in range(bw.steps)])
         bytes_step += select_bytes(bw.beams, bw.vocab)
@@ -467,7 +483,7 @@ def run_gpu(args):
         e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3)
         h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 * args.e2e_layers
         d2h = ho.numel() * 2 * args.e2e_layers
-        e2e = {"value": ps.flops * args.e2e_layers * world / e2e_s / 1e12, "unit": UNIT,
+        e2e = {"value": job_throughput(ps.flops * args.e2e_layers, world, e2e_s) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "layers": args.e2e_layers}
 
