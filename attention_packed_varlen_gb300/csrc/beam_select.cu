@@ -797,6 +797,7 @@ __global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
   __shared__ Scratch sh;
   __shared__ int start[kMaxTiles + 1];  // first list entry of each tile's segment
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  uint32_t kmax = 0;  // largest score key this thread histograms
   for (int d = tid; d < kLocalBins; d += kFinalThreads) sh.lbins[d] = 0u;
   __syncthreads();
   grid_dep_wait();
@@ -843,7 +844,9 @@ __global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
           const int e = e0 + k * kFinalThreads + tid;
           if (e < count) {
             cand[e] = v[k];
-            const uint32_t bin = score_key(v[k], cum, lse) >> 16;
+            const uint32_t sk = score_key(v[k], cum, lse);
+            kmax = max(kmax, sk);
+            const uint32_t bin = sk >> 16;
             const uint32_t d = top_bin - bin;
             if (d < static_cast<uint32_t>(kLocalBins)) atomicAdd(&sh.lbins[d], 1u);
             else red_add(p.fine + bin, 1u);
@@ -895,7 +898,9 @@ __global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
         }
         const unsigned long long entry = __ldcg(seg + static_cast<int64_t>(lo) * p.seg_cap + (e - start[lo]));
         cand[e] = entry;
-        const uint32_t bin = score_key(entry, cum, lse) >> 16;
+        const uint32_t sk = score_key(entry, cum, lse);
+        kmax = max(kmax, sk);
+        const uint32_t bin = sk >> 16;
         const uint32_t d = top_bin - bin;
         if (d < static_cast<uint32_t>(kLocalBins)) atomicAdd(&sh.lbins[d], 1u);
         else red_add(p.fine + bin, 1u);
@@ -914,7 +919,9 @@ __global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
     exact_beam(p, sh, b);
     count = p.K;
     for (int i = tid; i < count; i += kFinalThreads) {
-      const uint32_t bin = score_key(__ldcg(cand + i), cum, lse) >> 16;
+      const uint32_t sk = score_key(__ldcg(cand + i), cum, lse);
+      kmax = max(kmax, sk);
+      const uint32_t bin = sk >> 16;
       const uint32_t d = top_bin - bin;
       if (d < static_cast<uint32_t>(kLocalBins)) atomicAdd(&sh.lbins[d], 1u);
       else red_add(p.fine + bin, 1u);
@@ -927,7 +934,10 @@ __global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
     const unsigned v = sh.lbins[d];
     if (v) red_add(p.fine + (top_bin - d), v);
   }
-  if (tid == 0) atomicMax(p.misc + kMiscMaxKey, top_key);
+  // the global walk starts at the largest key actually histogrammed (with
+  // finite logits that is top_key; it also bounds NaN-derived keys)
+  kmax = warp_max_u32(kmax);
+  if (lane == 0) atomicMax(p.misc + kMiscMaxKey, kmax);
 }
 
 // ---------------------------------------------------------------------------
@@ -943,10 +953,11 @@ struct FinalHead {
   int fill[kRankBins];  // entries placed so far in bin S - d
 };
 
-__device__ __forceinline__ void write_result(const Params& p, int r, const ulonglong2& g) {
-  const int token = static_cast<int>(0xFFFFFFFFull - g.y);
-  const int parent = 0xFFFF - static_cast<int>((g.x >> 16) & 0xFFFFull);
-  const float score = key_to_f32(static_cast<uint32_t>(g.x >> 32));
+// Result r of the global order; error = true writes -1 ids and NaN scores.
+__device__ __forceinline__ void write_result(const Params& p, int r, const ulonglong2& g, bool error = false) {
+  const int token = error ? -1 : static_cast<int>(0xFFFFFFFFull - g.y);
+  const int parent = error ? -1 : 0xFFFF - static_cast<int>((g.x >> 16) & 0xFFFFull);
+  const float score = error ? __int_as_float(0x7fc00000) : key_to_f32(static_cast<uint32_t>(g.x >> 32));
   if (r < p.W) {
     p.out_token[r] = token;
     p.out_parent[r] = parent;
@@ -1048,16 +1059,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
   const unsigned status = __ldcg(p.misc + kMiscStatus);
   const int n_e = static_cast<int>(__ldcg(p.misc + kMiscElite));
   if (status != 0u || bstar < 0 || n_e < K) {
-    for (int r = tid; r < K; r += kFinalThreads) {
-      if (r < p.W) {
-        p.out_token[r] = -1;
-        p.out_parent[r] = -1;
-        p.out_score[r] = __int_as_float(0x7fc00000);
-      }
-      if (p.out_cand_token) p.out_cand_token[r] = -1;
-      if (p.out_cand_parent) p.out_cand_parent[r] = -1;
-      if (p.out_cand_score) p.out_cand_score[r] = __int_as_float(0x7fc00000);
-    }
+    for (int r = tid; r < K; r += kFinalThreads) write_result(p, r, make_ulonglong2(0ull, 0ull), true);
     return;
   }
 
@@ -1068,11 +1070,16 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
     unsigned long long* ehi = reinterpret_cast<unsigned long long*>(ent);
     uint32_t* elo = reinterpret_cast<uint32_t*>(ehi + cap);
     for (int d = tid; d <= S - bstar; d += kFinalThreads) fs.fill[d] = 0;
+    if (tid == 0) sh.counter = 0;  // entries outside [B*, S]: none unless the histogram is inconsistent
     __syncthreads();
     for (int i = tid; i < n_e; i += kFinalThreads) {
       const unsigned long long hi = __ldcg(&p.elite[i].x);
       const uint32_t lo = static_cast<uint32_t>(__ldcg(&p.elite[i].y));
       const int d = S - static_cast<int>(hi >> 48);
+      if (d < 0 || d > S - bstar) {
+        atomicAdd(&sh.counter, 1);
+        continue;
+      }
       const int idx = fs.pre[d] + atomicAdd(&fs.fill[d], 1);
       if (idx < cap) {
         ehi[idx] = hi;
@@ -1080,6 +1087,10 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
       }
     }
     __syncthreads();
+    if (sh.counter != 0) {
+      for (int r = tid; r < K; r += kFinalThreads) write_result(p, r, make_ulonglong2(0ull, 0ull), true);
+      return;
+    }
     for (int i = tid; i < n_e; i += kFinalThreads) {
       const unsigned long long hi = ehi[i];
       const uint32_t lo = elo[i];

@@ -67,3 +67,18 @@ def test_select_repeatable():
     b = slm.slm_beam_select(s.logits.to(dev), s.cum.to(dev), 100)
     for key in a:
         assert torch.equal(a[key], b[key]), key
+
+
+def test_sampled_threshold_miss():
+    # A row whose few very large logits sit exactly where the threshold's
+    # sample looks: the sample then overstates the row's top, fewer than 2W
+    # logits pass the threshold, and the beam must be redone exactly.  The
+    # sample positions are those of the 16-byte runs the selection reads
+    # (512 runs of 8 logits, evenly spaced, 8-aligned).
+    W_in, V, W = 8, 151936, 100
+    s = wl.select_inputs(W_in, V, W, seed=77)
+    logits = s.logits.clone()
+    runs = [(j * (V - 8) // 511) & ~7 for j in range(30)]
+    for b in range(W_in):
+        logits[b, runs] = 20.0
+    run_and_check(logits, s.cum, W)
