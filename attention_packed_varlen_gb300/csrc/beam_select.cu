@@ -617,7 +617,7 @@ struct Scratch {
   unsigned long long wu64[2][kFinalWarps];
   float wf[kFinalWarps];
   int wint[kFinalWarps];
-  int digit, above, in_bin, counter, flag, bstar, bstar_above;
+  int digit, above, in_bin, counter, flag, bstar, bstar_above, bstar_count;
   unsigned long long u64;
 };
 
@@ -628,6 +628,16 @@ __device__ __forceinline__ float block_max(float v, Scratch& sh) {
   __syncthreads();
   float r = sh.wf[0];
   for (int i = 1; i < kFinalWarps; ++i) r = fmaxf(r, sh.wf[i]);
+  return r;
+}
+
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Scratch& sh) {
+  v = warp_max_u32(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh.wint[threadIdx.x >> 5] = static_cast<int>(v);
+  __syncthreads();
+  uint32_t r = 0;
+  for (int i = 0; i < kFinalWarps; ++i) r = max(r, static_cast<uint32_t>(sh.wint[i]));
   return r;
 }
 
@@ -912,12 +922,15 @@ __global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
     if (p.out_lse) p.out_lse[b] = lse;
   }
   // the row maximum is a candidate, so its score is the beam's largest
-  const uint32_t top_key = f32_key(__fadd_rn(cum, __fsub_rn(top, lse)));
-  const uint32_t top_bin = top_key >> 16;
+  uint32_t top_bin = f32_key(__fadd_rn(cum, __fsub_rn(top, lse))) >> 16;
   if (over || count < p.K || count > kCap) {
     // the threshold missed: the exact top K from the whole row
     exact_beam(p, sh, b);
     count = p.K;
+    for (int i = tid; i < count; i += kFinalThreads) kmax = max(kmax, score_key(__ldcg(cand + i), cum, lse));
+    // the window starts at the largest key of the exact list itself
+    const uint32_t kb = block_max_u32(kmax, sh);
+    top_bin = kb >> 16;
     for (int i = tid; i < count; i += kFinalThreads) {
       const uint32_t sk = score_key(__ldcg(cand + i), cum, lse);
       kmax = max(kmax, sk);
@@ -935,7 +948,7 @@ __global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
     if (v) red_add(p.fine + (top_bin - d), v);
   }
   // the global walk starts at the largest key actually histogrammed (with
-  // finite logits that is top_key; it also bounds NaN-derived keys)
+  // finite logits that of the row maximum; it also bounds NaN-derived keys)
   kmax = warp_max_u32(kmax);
   if (lane == 0) atomicMax(p.misc + kMiscMaxKey, kmax);
 }
@@ -1005,6 +1018,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
       if (carry + excl < K && carry + excl + c >= K) {
         sh.bstar = bin;
         sh.bstar_above = carry + excl;
+        sh.bstar_count = c;
       }
       carry += total;
       if (carry >= K || top - kFinalThreads < 0) break;
@@ -1058,7 +1072,8 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
 
   const unsigned status = __ldcg(p.misc + kMiscStatus);
   const int n_e = static_cast<int>(__ldcg(p.misc + kMiscElite));
-  if (status != 0u || bstar < 0 || n_e < K) {
+  // the list holds exactly the histogram's entries in bins >= B*
+  if (status != 0u || bstar < 0 || n_e < K || n_e != sh.bstar_above + sh.bstar_count) {
     for (int r = tid; r < K; r += kFinalThreads) write_result(p, r, make_ulonglong2(0ull, 0ull), true);
     return;
   }
@@ -1097,8 +1112,9 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
       const int d = S - static_cast<int>(hi >> 48);
       const int g0 = fs.pre[d], gn = fs.fill[d];
       int rank = g0;
+      const int g1 = min(g0 + gn, n_e);
 #pragma unroll 4
-      for (int j = g0; j < g0 + gn; ++j) {
+      for (int j = g0; j < g1; ++j) {
         const unsigned long long hj = ehi[j];
         rank += (hj > hi) | ((hj == hi) & (elo[j] > lo));
       }
