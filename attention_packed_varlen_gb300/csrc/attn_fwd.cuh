@@ -73,9 +73,13 @@ template <int D>
 struct FwdSmem {
   static constexpr int kDSub = D / 64;
   static constexpr int kTile = kDSub * kSubTileBytes;  // 128 rows x D bf16
-  static constexpr int kStages = (D == 128) ? 3 : 6;   // K/V ring
-  static constexpr int kQ = 0;                         // [2 buffers][2 sub-tiles]
-  static constexpr int kKV = kQ + 4 * kTile;
+  // D = 128: one Q buffer, released as soon as the unit's last S MMA is done,
+  // so the K/V ring can hold 2.5 blocks and the next unit's first blocks
+  // arrive while the current unit ends.  D = 64: two Q buffers, 5 blocks.
+  static constexpr int kQBufs = (D == 128) ? 1 : 2;
+  static constexpr int kStages = (D == 128) ? 5 : 10;  // K/V ring
+  static constexpr int kQ = 0;                         // [kQBufs buffers][2 sub-tiles]
+  static constexpr int kKV = kQ + 2 * kQBufs * kTile;
   static constexpr int kBar = kKV + kStages * kTile;
   // barrier slots
   static constexpr int Q_FULL = 0, Q_EMPTY = 2, KV_FULL = 4, KV_EMPTY = KV_FULL + kStages,
@@ -209,7 +213,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // hold finite values: zero them once.
   if (rows_used < kBlockM) {
     const int tail = kBlockM - rows_used;
-    for (int i = threadIdx.x; i < 4 * L::kDSub * tail * 8; i += kFwdThreads) {
+    for (int i = threadIdx.x; i < 2 * L::kQBufs * L::kDSub * tail * 8; i += kFwdThreads) {
       const int chunk = i & 7;
       int rest = i >> 3;
       const int r = rows_used + rest % tail;
@@ -244,8 +248,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const UnitInfo U = unit_info<MODE>(p, u, rn);
         if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
         if (U.nblk_max == 0) continue;  // decode with an empty prefix: suffix only
-        const int qb = qi & 1;
-        if (qi >= 2) ok = mbar_wait(&bars[L::Q_EMPTY + qb], ((qi >> 1) - 1) & 1, abort_flag);
+        const int qb = qi % L::kQBufs;
+        if (qi >= L::kQBufs) ok = mbar_wait(&bars[L::Q_EMPTY + qb], ((qi / L::kQBufs) - 1) & 1, abort_flag);
         if (!ok) break;
         uint32_t q_bytes = 0;
         for (int t = 0; t < 2; ++t)
@@ -259,7 +263,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         ++qi;
       }
       if (!ok)  // let the copies already issued land before shared memory is released
-        for (int i = qi > 2 ? qi - 2 : 0; i < qi; ++i) mbar_wait_drain(&bars[L::Q_FULL + (i & 1)], (i >> 1) & 1);
+        for (int i = qi > L::kQBufs ? qi - L::kQBufs : 0; i < qi; ++i)
+          mbar_wait_drain(&bars[L::Q_FULL + (i % L::kQBufs)], (i / L::kQBufs) & 1);
     } else if (lane == 0) {
       uint32_t kv_i = 0;
       bool ok = true;
@@ -317,8 +322,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // the next unit's item loads while this one runs
         if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
         if (U.nblk_max == 0) continue;
-        const int qb = it & 1;
-        ok = mbar_wait(&bars[L::Q_FULL + qb], (it >> 1) & 1, abort_flag);
+        const int qb = it % L::kQBufs;
+        ok = mbar_wait(&bars[L::Q_FULL + qb], (it / L::kQBufs) & 1, abort_flag);
         const uint32_t kbase = kv_i;
         if (ok) ok = mbar_wait(&bars[L::KV_FULL + slot(kbase)], phase(kbase), abort_flag);
         if (!ok) break;
@@ -329,6 +334,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             umma_commit(&bars[L::S_FULL + t]);
           }
         umma_commit(&bars[L::KV_EMPTY + slot(kbase)]);
+        if (U.nblk_max == 1) umma_commit(&bars[L::Q_EMPTY + qb]);  // the unit's last S MMAs are issued
         for (int j = 0; j < U.nblk_max && ok; ++j) {
           const uint32_t vi = kbase + 2 * j + 1, kn = kbase + 2 * j + 2;
           ok = mbar_wait(&bars[L::KV_FULL + slot(vi)], phase(vi), abort_flag);
@@ -358,9 +364,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           if (!ok) break;
           umma_commit(&bars[L::KV_EMPTY + slot(vi)]);
           if (j + 1 < U.nblk_max) umma_commit(&bars[L::KV_EMPTY + slot(kn)]);
+          // the Q buffer is free once the unit's last S MMAs complete
+          if (j + 1 == U.nblk_max - 1) umma_commit(&bars[L::Q_EMPTY + qb]);
         }
         kv_i = kbase + 2 * U.nblk_max;
-        umma_commit(&bars[L::Q_EMPTY + qb]);
         ++it;
       }
       // All MMAs issued by this thread complete before TMEM can be released.
