@@ -95,14 +95,14 @@ int num_sms() {
 
 // Persistent launch: one CTA per SM (or per unit when there are fewer).
 template <int D, AttnMode MODE>
-cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const AttnParams& p,
-                        int64_t max_units, cudaStream_t stream) {
+cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                        const AttnParams& p, int64_t max_units, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, MODE>;
   const int smem = FwdSmem<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), max_units)));
-  kern<<<grid, kFwdThreads, smem, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kFwdThreads, smem, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
@@ -252,8 +252,9 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   const int tok = kBlockM / G;
   const int64_t cap = prefill_item_capacity(num_seqs, total_tokens, tok);
   if (cap * n_kv_heads > 0x7FFFFFFF) return fail(SLM_ERR_UNSUPPORTED, "too many tiles");
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_bf16_3d(&tq, q, head_dim, n_q_heads, total_tokens, G, tok) ||
+      !encode_bf16_3d(&to, o, head_dim, n_q_heads, total_tokens, G, tok) ||
       !encode_bf16_3d(&tk, k, head_dim, n_kv_heads, total_tokens, 1, kBlockN) ||
       !encode_bf16_3d(&tv, v, head_dim, n_kv_heads, total_tokens, 1, kBlockN))
     return fail(SLM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
@@ -277,8 +278,8 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   p.cu_seqlens = cu_seqlens;
   p.items = items;
   p.total_tokens = total_tokens;
-  e = (head_dim == 64) ? launch_attn<64, AttnMode::kPrefill>(tq, tk, tv, p, cap * n_kv_heads, stream)
-                       : launch_attn<128, AttnMode::kPrefill>(tq, tk, tv, p, cap * n_kv_heads, stream);
+  e = (head_dim == 64) ? launch_attn<64, AttnMode::kPrefill>(tq, tk, tv, to, p, cap * n_kv_heads, stream)
+                       : launch_attn<128, AttnMode::kPrefill>(tq, tk, tv, to, p, cap * n_kv_heads, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   return ok();
 }
@@ -348,8 +349,10 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
   p.Lp = Lp;
   p.L_prev = L_prev;
   p.Smax = Smax;
-  cudaError_t e = (head_dim == 64) ? launch_attn<64, AttnMode::kDecodePrefix>(tq, tk, tv, p, n_units, stream)
-                                   : launch_attn<128, AttnMode::kDecodePrefix>(tq, tk, tv, p, n_units, stream);
+  // decode writes O row by row (the suffix merge ends in registers); the
+  // output map argument is unused
+  cudaError_t e = (head_dim == 64) ? launch_attn<64, AttnMode::kDecodePrefix>(tq, tk, tv, tq, p, n_units, stream)
+                                   : launch_attn<128, AttnMode::kDecodePrefix>(tq, tk, tv, tq, p, n_units, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   return ok();
 }

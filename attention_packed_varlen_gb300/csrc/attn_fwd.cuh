@@ -74,13 +74,15 @@ struct FwdSmem {
   static constexpr int kDSub = D / 64;
   static constexpr int kTile = kDSub * kSubTileBytes;  // 128 rows x D bf16
   // D = 128: one Q buffer, released as soon as the unit's last S MMA is done,
-  // so the K/V ring can hold 2.5 blocks and the next unit's first blocks
-  // arrive while the current unit ends.  D = 64: two Q buffers, 5 blocks.
+  // so the K/V ring can hold 2 blocks and the next unit's first blocks
+  // arrive while the current unit ends.  D = 64: two Q buffers, 4 blocks.
+  // Both: 32 KB to stage O for TMA stores.
   static constexpr int kQBufs = (D == 128) ? 1 : 2;
-  static constexpr int kStages = (D == 128) ? 5 : 10;  // K/V ring
+  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring
   static constexpr int kQ = 0;                         // [kQBufs buffers][2 sub-tiles]
   static constexpr int kKV = kQ + 2 * kQBufs * kTile;
-  static constexpr int kBar = kKV + kStages * kTile;
+  static constexpr int kOut = kKV + kStages * kTile;   // [2 sub-tiles] 128 rows x 64 bf16: O staging for TMA stores
+  static constexpr int kBar = kOut + 2 * kSubTileBytes;
   // barrier slots
   static constexpr int Q_FULL = 0, Q_EMPTY = 2, KV_FULL = 4, KV_EMPTY = KV_FULL + kStages,
                        S_FULL = KV_EMPTY + kStages, P_FULL = S_FULL + 2, O_FULL = P_FULL + 2,
@@ -165,7 +167,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <int D, AttnMode MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const AttnParams p) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -204,6 +207,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
   if (warp == 8 && lane == 0) {
     tma_prefetch_desc(&tm_q);
+    if (MODE == AttnMode::kPrefill) tma_prefetch_desc(&tm_o);
     if (MODE == AttnMode::kPrefill || p.Lp > 0) {  // the K/V maps are left empty when there is no prefix
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -560,18 +564,50 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
 
+      const bool tma_out = (MODE == AttnMode::kPrefill) && U.n_tok[t] == TOK;
+      if (tma_out) {
+        // A full sub-tile: rows staged in shared memory in the swizzled box
+        // layout (row r = token * G + head, as the Q tile), 64 columns at a
+        // time, and written by one TMA store each -- whole lines instead of
+        // 16-byte pieces of 256-byte rows.
+        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        uint8_t* stage = smem + L::kOut + t * kSubTileBytes;
+#pragma unroll
+        for (int dh = 0; dh < L::kDSub; ++dh) {
+          if (r == 0) bulk_wait_read0();  // the previous store has read the staging buffer
+          named_bar_sync(1 + t, 128);
+          if (r < rows_used) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int d = dh * 64 + c * 8;
+              st_shared_v4(smem_u32(stage + sw128_offset(r, c * 8)), pack_bf16x2(acc[d + 0] * inv_l, acc[d + 1] * inv_l),
+                           pack_bf16x2(acc[d + 2] * inv_l, acc[d + 3] * inv_l),
+                           pack_bf16x2(acc[d + 4] * inv_l, acc[d + 5] * inv_l),
+                           pack_bf16x2(acc[d + 6] * inv_l, acc[d + 7] * inv_l));
+            }
+          }
+          fence_proxy_async_smem();
+          named_bar_sync(1 + t, 128);
+          if (r == 0) {
+            tma_store_3d(&tm_o, stage, dh * 64, U.kvh * G, U.row0[t]);
+            bulk_commit();
+          }
+        }
+      }
       if (row_valid) {
         const float inv_l = 1.f / l_run;
         const int64_t out_row = static_cast<int64_t>(rowid) * p.n_q_heads + h;
-        uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
+        if (!tma_out) {
+          uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
 #pragma unroll
-        for (int d = 0; d < D; d += 8) {
-          uint4 v;
-          v.x = pack_bf16x2(acc[d + 0] * inv_l, acc[d + 1] * inv_l);
-          v.y = pack_bf16x2(acc[d + 2] * inv_l, acc[d + 3] * inv_l);
-          v.z = pack_bf16x2(acc[d + 4] * inv_l, acc[d + 5] * inv_l);
-          v.w = pack_bf16x2(acc[d + 6] * inv_l, acc[d + 7] * inv_l);
-          dst[d >> 3] = v;
+          for (int d = 0; d < D; d += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(acc[d + 0] * inv_l, acc[d + 1] * inv_l);
+            v.y = pack_bf16x2(acc[d + 2] * inv_l, acc[d + 3] * inv_l);
+            v.z = pack_bf16x2(acc[d + 4] * inv_l, acc[d + 5] * inv_l);
+            v.w = pack_bf16x2(acc[d + 6] * inv_l, acc[d + 7] * inv_l);
+            dst[d >> 3] = v;
+          }
         }
         if (p.lse) {
           const float lse = (m_run + __log2f(l_run)) * 0.69314718055994531f;
@@ -612,6 +648,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 
   // ---- teardown ----
+  if (MODE == AttnMode::kPrefill && warp < 8 && (threadIdx.x & 127) == 0) bulk_wait_all0();  // TMA stores done
   tc_fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag && p.dev_status) atomicOr(p.dev_status, kDevPipelineTimeout);
