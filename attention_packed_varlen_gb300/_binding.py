@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "SLM_OK", 1: "SLM_ERR_INVALID_ARG", 2: "SLM_ERR_UNSUPPORTED",
 
 EXPORTS = ("slm_last_error", "slm_abi_version", "slm_packed_prefill_attn", "slm_prefill_workspace_size",
            "slm_shared_prefix_decode_attn", "slm_beam_select", "slm_beam_select_workspace_size",
-           "slm_check_status", "slm_packed_prefill_attn_noalloc")
+           "slm_check_status", "slm_packed_prefill_attn_noalloc", "slm_swiglu_quant_e4m3", "slm_label_scores",
+           "slm_beam_split_finished", "slm_beam_reorder_history")
 
 
 class SlmError(RuntimeError):
@@ -68,6 +69,14 @@ def load(path: Optional[str] = None):
         lib.slm_check_status.argtypes = [P, P]
         lib.slm_packed_prefill_attn_noalloc.restype = ctypes.c_int
         lib.slm_packed_prefill_attn_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, P]
+        lib.slm_swiglu_quant_e4m3.restype = ctypes.c_int
+        lib.slm_swiglu_quant_e4m3.argtypes = [P, i32, i32, P, P, P]
+        lib.slm_label_scores.restype = ctypes.c_int
+        lib.slm_label_scores.argtypes = [P, P, i32, i32, i32, P, i32, P, P, P, P]
+        lib.slm_beam_split_finished.restype = ctypes.c_int
+        lib.slm_beam_split_finished.argtypes = [P, P, P, i32, i32, P, P, P, P, P, P, P, P]
+        lib.slm_beam_reorder_history.restype = ctypes.c_int
+        lib.slm_beam_reorder_history.argtypes = [P, P, P, i32, i32, i32, i32, P, P, P]
         if path is None:
             _lib = lib
         return lib
@@ -243,3 +252,76 @@ def slm_beam_select(logits: torch.Tensor, cum_scores: torch.Tensor, W: int, *, w
 def slm_check_status(dev_status: torch.Tensor) -> None:
     _need(dev_status, "dev_status", torch.int32)
     _check(load().slm_check_status(_ptr(dev_status), _stream(dev_status.device)))
+
+
+# ----------------------------------------------------------------------------
+# MLP: fused SwiGLU + per-token E4M3
+# ----------------------------------------------------------------------------
+def slm_swiglu_quant_e4m3(gate_up: torch.Tensor):
+    """Returns (q uint8 [T, I] E4M3 codes, scale fp32 [T]) for gate_up bf16 [T, 2I]."""
+    _need(gate_up, "gate_up", torch.bfloat16, 2)
+    T, two_i = gate_up.shape
+    if two_i % 2:
+        raise ValueError("gate_up must have an even number of columns")
+    I = two_i // 2
+    q = torch.empty((T, I), dtype=torch.uint8, device=gate_up.device)
+    scale = torch.empty(T, dtype=torch.float32, device=gate_up.device)
+    _check(load().slm_swiglu_quant_e4m3(_ptr(gate_up), T, I, _ptr(q), _ptr(scale), _stream(gate_up.device)))
+    return q, scale
+
+
+# ----------------------------------------------------------------------------
+# Prefill-Only: last-token label scores
+# ----------------------------------------------------------------------------
+def slm_label_scores(hidden: torch.Tensor, cu_seqlens: torch.Tensor, w_label: torch.Tensor, *,
+                     dev_status: Optional[torch.Tensor] = None, want_probs: bool = True):
+    """Returns (logits, probs) fp32 [num_seqs, n_labels] (probs None when not wanted)."""
+    _need(hidden, "hidden", torch.bfloat16, 2)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(w_label, "w_label", torch.bfloat16, 2)
+    T, d = hidden.shape
+    n_labels = w_label.shape[0]
+    if w_label.shape[1] != d:
+        raise ValueError("w_label must be [n_labels, d_model]")
+    B = cu_seqlens.numel() - 1
+    dev = hidden.device
+    logits = torch.empty((B, n_labels), dtype=torch.float32, device=dev)
+    probs = torch.empty((B, n_labels), dtype=torch.float32, device=dev) if want_probs else None
+    _check(load().slm_label_scores(_ptr(hidden), _ptr(cu_seqlens), B, T, d, _ptr(w_label), n_labels, _ptr(logits),
+                                   _ptr(probs), _ptr(dev_status), _stream(dev)))
+    return logits, probs
+
+
+# ----------------------------------------------------------------------------
+# Beam search state: finished hypotheses, token history
+# ----------------------------------------------------------------------------
+def slm_beam_split_finished(cand_token: torch.Tensor, cand_parent: torch.Tensor, cand_score: torch.Tensor,
+                            stop_id: int):
+    """Returns dict(token, parent, score [W]: active beams; fin_token, fin_parent, fin_score [W] and
+    fin_count [1]: hypotheses finished at this step)."""
+    _need(cand_token, "cand_token", torch.int32, 1)
+    _need(cand_parent, "cand_parent", torch.int32, 1)
+    _need(cand_score, "cand_score", torch.float32, 1)
+    W = cand_token.numel() // 2
+    dev = cand_token.device
+    res = {k: torch.empty(W, dtype=torch.int32, device=dev) for k in ("token", "parent", "fin_token", "fin_parent")}
+    res["score"] = torch.empty(W, dtype=torch.float32, device=dev)
+    res["fin_score"] = torch.empty(W, dtype=torch.float32, device=dev)
+    res["fin_count"] = torch.empty(1, dtype=torch.int32, device=dev)
+    _check(load().slm_beam_split_finished(
+        _ptr(cand_token), _ptr(cand_parent), _ptr(cand_score), W, stop_id, _ptr(res["token"]), _ptr(res["parent"]),
+        _ptr(res["score"]), _ptr(res["fin_token"]), _ptr(res["fin_parent"]), _ptr(res["fin_score"]),
+        _ptr(res["fin_count"]), _stream(dev)))
+    return res
+
+
+def slm_beam_reorder_history(hist_in: Optional[torch.Tensor], parent: Optional[torch.Tensor], token: torch.Tensor,
+                             t: int, hist_out: torch.Tensor, *, dev_status: Optional[torch.Tensor] = None):
+    """hist_out[b, :t] = hist_in[parent[b], :t]; hist_out[b, t] = token[b]."""
+    _need(token, "token", torch.int32, 1)
+    _need(hist_out, "hist_out", torch.int32, 2)
+    W, max_len = hist_out.shape
+    W_in = hist_in.shape[0] if hist_in is not None else 1
+    _check(load().slm_beam_reorder_history(_ptr(hist_in), _ptr(parent), _ptr(token), W, W_in, t, max_len,
+                                           _ptr(hist_out), _ptr(dev_status), _stream(token.device)))
+    return hist_out

@@ -25,6 +25,18 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
                                int32_t* out_cand_parent, float* out_cand_score, float* out_lse, void* workspace,
                                cudaStream_t stream);
 
+// Defined in heads.cu
+cudaError_t launch_swiglu_quant(const void* gate_up, int T, int I, void* q, float* scale, int num_sms,
+                                cudaStream_t stream);
+cudaError_t launch_label_scores(const void* hidden, const int32_t* cu, int B, int T, int d, const void* w_label,
+                                int n_labels, float* logits, float* probs, int32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_beam_finished(const int32_t* cand_token, const int32_t* cand_parent, const float* cand_score, int W,
+                                 int stop_id, int32_t* out_token, int32_t* out_parent, float* out_score,
+                                 int32_t* fin_token, int32_t* fin_parent, float* fin_score, int32_t* fin_count,
+                                 cudaStream_t stream);
+cudaError_t launch_beam_history(const int32_t* hist_in, const int32_t* parent, const int32_t* token, int W, int W_in,
+                                int t, int max_len, int32_t* hist_out, int32_t* dev_status, cudaStream_t stream);
+
 namespace {
 
 thread_local std::string g_last_error;
@@ -383,6 +395,65 @@ slm_status slm_beam_select(const void* logits, const float* cum_scores, int32_t 
   cudaError_t e = launch_beam_select(logits, cum_scores, W_in, V, W, out_token, out_parent, out_score,
                                      out_cand_token, out_cand_parent, out_cand_score, out_lse, workspace, stream);
   if (e != cudaSuccess) return cuda_fail(e, "beam select launch");
+  return ok();
+}
+
+slm_status slm_swiglu_quant_e4m3(const void* gate_up, int32_t T, int32_t I, void* q, float* scale, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (T < 0 || I <= 0) return fail(SLM_ERR_INVALID_ARG, "need T >= 0 and I > 0 (T=%d I=%d)", T, I);
+  if (I % 8 != 0) return fail(SLM_ERR_UNSUPPORTED, "I=%d must be a multiple of 8", I);
+  if (T == 0) return ok();
+  if (!gate_up || !q || !scale) return fail(SLM_ERR_INVALID_ARG, "null gate_up/q/scale");
+  if (!aligned16(gate_up) || !aligned16(q) || !aligned16(scale))
+    return fail(SLM_ERR_INVALID_ARG, "gate_up/q/scale must be 16-byte aligned");
+  cudaError_t e = launch_swiglu_quant(gate_up, T, I, q, scale, num_sms(), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "swiglu quant launch");
+  return ok();
+}
+
+slm_status slm_label_scores(const void* hidden, const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                            int32_t d_model, const void* w_label, int32_t n_labels, float* logits, float* probs,
+                            int32_t* dev_status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (num_seqs < 0 || total_tokens < 0 || d_model <= 0)
+    return fail(SLM_ERR_INVALID_ARG, "bad sizes (num_seqs=%d total_tokens=%d d_model=%d)", num_seqs, total_tokens,
+                d_model);
+  if (n_labels < 1 || n_labels > 32) return fail(SLM_ERR_UNSUPPORTED, "n_labels=%d outside [1, 32]", n_labels);
+  if (d_model % 8 != 0) return fail(SLM_ERR_UNSUPPORTED, "d_model=%d must be a multiple of 8", d_model);
+  if (num_seqs == 0) return ok();
+  if (!hidden || !cu_seqlens || !w_label || !logits) return fail(SLM_ERR_INVALID_ARG, "null hidden/cu_seqlens/w_label/logits");
+  if (!aligned16(hidden) || !aligned16(w_label)) return fail(SLM_ERR_INVALID_ARG, "hidden/w_label must be 16-byte aligned");
+  cudaError_t e = launch_label_scores(hidden, cu_seqlens, num_seqs, total_tokens, d_model, w_label, n_labels, logits,
+                                      probs, dev_status, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "label scores launch");
+  return ok();
+}
+
+slm_status slm_beam_split_finished(const int32_t* cand_token, const int32_t* cand_parent, const float* cand_score,
+                                   int32_t W, int32_t stop_id, int32_t* out_token, int32_t* out_parent,
+                                   float* out_score, int32_t* fin_token, int32_t* fin_parent, float* fin_score,
+                                   int32_t* fin_count, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (W < 1 || W > 1024) return fail(SLM_ERR_INVALID_ARG, "W=%d outside [1, 1024]", W);
+  if (!cand_token || !cand_parent || !cand_score || !out_token || !out_parent || !out_score || !fin_token ||
+      !fin_parent || !fin_score || !fin_count)
+    return fail(SLM_ERR_INVALID_ARG, "null pointer argument");
+  cudaError_t e = launch_beam_finished(cand_token, cand_parent, cand_score, W, stop_id, out_token, out_parent, out_score,
+                                       fin_token, fin_parent, fin_score, fin_count, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "finished split launch");
+  return ok();
+}
+
+slm_status slm_beam_reorder_history(const int32_t* hist_in, const int32_t* parent_idx, const int32_t* token,
+                                    int32_t W, int32_t W_in, int32_t t, int32_t max_len, int32_t* hist_out,
+                                    int32_t* dev_status, void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  if (W < 1 || W_in < 1 || t < 0 || max_len < 1 || t >= max_len)
+    return fail(SLM_ERR_INVALID_ARG, "bad sizes (W=%d W_in=%d t=%d max_len=%d)", W, W_in, t, max_len);
+  if (!token || !hist_out || (t > 0 && !hist_in)) return fail(SLM_ERR_INVALID_ARG, "null token/hist_out/hist_in");
+  if (hist_in == hist_out) return fail(SLM_ERR_INVALID_ARG, "hist_out aliases hist_in");
+  cudaError_t e = launch_beam_history(hist_in, parent_idx, token, W, W_in, t, max_len, hist_out, dev_status, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "history reorder launch");
   return ok();
 }
 

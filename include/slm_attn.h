@@ -154,6 +154,92 @@ slm_status slm_beam_select(const void* logits, const float* cum_scores, int32_t 
 size_t slm_beam_select_workspace_size(int32_t W_in, int32_t V, int32_t W);
 
 /*
+ * Fused SwiGLU and per-token dynamic E4M3 re-quantisation (article section
+ * 3.4, the MLP data path between the FP8 Gate/Up and Down GEMMs): one pass
+ * per token row, without a BF16 SwiGLU intermediate.
+ *
+ *   gate_up bf16 [T, 2*I]: row t holds gate_t [I] then up_t [I] (the Gate/Up
+ *           GEMM output);
+ *   q       E4M3 (OCP FP8, one byte per element) [T, I]: codes of
+ *           h_t * (448 / amax_t), rounded to nearest even and saturated to
+ *           +-448, where h_t = SiLU(gate_t) * up_t in FP32 and amax_t =
+ *           max |h_t|;
+ *   scale   fp32 [T]: amax_t / 448 (so h_t ~= code * scale); a row with
+ *           amax_t = 0 gets scale 1 and all-zero codes.
+ *
+ * Requires I % 8 == 0.  No workspace.
+ */
+slm_status slm_swiglu_quant_e4m3(const void* gate_up, int32_t T, int32_t I, void* q, float* scale, void* stream);
+
+/*
+ * Last-valid-token extraction and label scoring for Prefill-Only models
+ * (article sections 1.1 and 3.1): the same sequence boundary as the packed
+ * prefill selects each sequence's last row of hidden states; its next-token
+ * logits are computed for the label tokens only, and a softmax over the
+ * labels gives the scores.
+ *
+ *   hidden     bf16 [total_tokens, d_model]: final hidden states, packed;
+ *   cu_seqlens int32 [num_seqs + 1] (device): sequence boundaries;
+ *   w_label    bf16 [n_labels, d_model]: the label tokens' rows of the
+ *              prediction head;
+ *   logits     fp32 [num_seqs, n_labels]: z_bk = sum_j h_b[j] * w_k[j], FP32
+ *              accumulation, h_b = hidden[cu_seqlens[b+1] - 1];
+ *   probs      fp32 [num_seqs, n_labels] (nullable): softmax of z_b over k.
+ *
+ * A sequence of length 0 gets NaN logits and probs.  A malformed boundary
+ * (decreasing, or outside [0, total_tokens]) gives NaN for that sequence and
+ * sets SLM_DEV_BAD_SEQLENS in *dev_status (nullable).  Requires
+ * 1 <= n_labels <= 32 and d_model % 8 == 0.
+ */
+slm_status slm_label_scores(const void* hidden, const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                            int32_t d_model, const void* w_label, int32_t n_labels, float* logits, float* probs,
+                            int32_t* dev_status, void* stream);
+
+/*
+ * Finished-beam handling with the 2W global candidates (article section
+ * 3.3: the intermediate step keeps 2W global candidates so that sequences
+ * that produced the stop token can be set aside while W active beams go on).
+ *
+ *   cand_token / cand_parent int32 [2W], cand_score fp32 [2W]: the global
+ *              candidates in order, as slm_beam_select writes them;
+ *   out_token / out_parent int32 [W], out_score fp32 [W]: the first W
+ *              candidates whose token is not stop_id, in order -- the next
+ *              active beams;
+ *   fin_token / fin_parent int32 [W], fin_score fp32 [W]: the candidates
+ *              ranked among the first W whose token is stop_id, in order --
+ *              the hypotheses finished at this step; fin_count int32 [1]:
+ *              how many.
+ *
+ * Each beam's row holds the stop token once, so at most W_in <= W
+ * candidates are stops and W active beams always remain.  Requires
+ * 1 <= W <= 1024.
+ */
+slm_status slm_beam_split_finished(const int32_t* cand_token, const int32_t* cand_parent, const float* cand_score,
+                                   int32_t W, int32_t stop_id, int32_t* out_token, int32_t* out_parent,
+                                   float* out_score, int32_t* fin_token, int32_t* fin_parent, float* fin_score,
+                                   int32_t* fin_count, void* stream);
+
+/*
+ * Token-history reorder of fixed-depth beam search (article section 2.3: the
+ * generated token sequence is one of the states the parent index reorders
+ * each step).
+ *
+ *   hist_in  int32 [W_in, max_len]: tokens of the current beams, columns
+ *            0..t-1 valid (may be NULL when t == 0);
+ *   parent_idx int32 [W] (device; NULL = identity): source beam of each new
+ *            beam, in [0, W_in);
+ *   token    int32 [W]: the new beams' tokens;
+ *   hist_out int32 [W, max_len]: hist_out[b, s] = hist_in[parent[b], s] for
+ *            s < t and hist_out[b, t] = token[b]; must not alias hist_in.
+ *
+ * A parent outside [0, W_in) reads row 0 and sets SLM_DEV_BAD_PARENT in
+ * *dev_status (nullable).  Requires 0 <= t < max_len.
+ */
+slm_status slm_beam_reorder_history(const int32_t* hist_in, const int32_t* parent_idx, const int32_t* token,
+                                    int32_t W, int32_t W_in, int32_t t, int32_t max_len, int32_t* hist_out,
+                                    int32_t* dev_status, void* stream);
+
+/*
  * slm_packed_prefill_attn without a workspace argument.  The article has no
  * counterpart; this entry point exists for callers that cannot allocate
  * device memory where they run attention (a frozen ahead-of-time compiled

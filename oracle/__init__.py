@@ -18,6 +18,9 @@ and marshals numpy / torch arrays into it.  Sources followed, from the article
   cumulative beam scores, global candidates from the flattened beams (here by
   a full sort of every W x V entry).
 
+The operations around the attention path (SwiGLU + E4M3, label scores,
+finished beams, the fixed-depth decode loop) are in ``oracle/heads.py``.
+
 Pins that tie this oracle to something other than itself are in
 ``tests/test_oracle_*.py``.
 """
