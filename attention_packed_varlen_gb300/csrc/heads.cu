@@ -313,7 +313,7 @@ __global__ void beam_history_kernel(const int32_t* __restrict__ hin, const int32
                                     int32_t* __restrict__ hout, int32_t* dev_status) {
   const int b = blockIdx.x;
   int src = parent ? parent[b] : b;
-  if (src < 0 || src >= W_in) {
+  if (t > 0 && (src < 0 || src >= W_in)) {  // at t = 0 no row is gathered
     if (threadIdx.x == 0 && dev_status) atomicOr(dev_status, kDevBadParent);
     src = 0;
   }

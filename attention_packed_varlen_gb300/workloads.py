@@ -233,3 +233,48 @@ def quantized_logits(W_in: int, V: int, levels: int, seed: int) -> torch.Tensor:
     rng = np.random.default_rng(int(seed))
     vals = rng.integers(0, levels, size=(W_in, V)).astype(np.float32) * 0.5
     return torch.from_numpy(vals).to(torch.bfloat16)
+
+
+# ----------------------------------------------------------------------------
+# Fixed-depth beam search loop inputs
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass
+class DecodeLoopInputs:
+    logits0: torch.Tensor        # bf16 [1, V]: the prompt's last-row logits
+    kp: torch.Tensor             # bf16 [Lp, Hkv, D]: shared prompt K/V
+    vp: torch.Tensor
+    steps: list                  # per decode step: (q [W, Hq, D], k_new [W, Hkv, D], v_new, logits [W, V])
+    stop_id: Optional[int]
+    softmax_scale: float
+
+
+def decode_loop_inputs(bw: BeamWorkload, seed: int, n_steps: Optional[int] = None,
+                       stop_id: Optional[int] = None, stop_rows: float = 0.0) -> DecodeLoopInputs:
+    """Synthetic inputs of the fixed-depth loop: prompt K/V, first-step logits,
+    and per decode step the new rows' q/k/v and the step's logits (the stand-in
+    for the prediction head, whose weights are not part of this path).  With a
+    stop id, a fraction `stop_rows` of each step's rows gets the stop token
+    among its highest logits (just above the row's maximum), so stop
+    candidates reach the global list."""
+    n_steps = bw.steps if n_steps is None else n_steps
+    W, V, Hq, Hkv, D = bw.beams, bw.vocab, bw.n_q_heads, bw.n_kv_heads, bw.head_dim
+    kp = bf16_randn((bw.prefix_len, Hkv, D), seed * 16 + 1)
+    vp = bf16_randn((bw.prefix_len, Hkv, D), seed * 16 + 2)
+    rng = np.random.default_rng(int(seed))
+
+    def logits_rows(n, s):
+        x = bf16_randn((n, V), s, bw.logit_std)
+        if stop_id is not None and stop_rows > 0:
+            rows = np.nonzero(rng.random(n) < stop_rows)[0]
+            if len(rows):
+                top = x[rows].float().max(dim=1).values
+                x[rows, stop_id] = (top + 0.5).to(torch.bfloat16)
+        return x
+
+    logits0 = logits_rows(1, seed * 16 + 3)
+    steps = []
+    for t in range(n_steps):
+        base = seed * 16 + 4 + 4 * t
+        steps.append((bf16_randn((W, Hq, D), base * 7 + 1), bf16_randn((W, Hkv, D), base * 7 + 2),
+                      bf16_randn((W, Hkv, D), base * 7 + 3), logits_rows(W, base * 7 + 4)))
+    return DecodeLoopInputs(logits0, kp, vp, steps, stop_id, bw.softmax_scale)

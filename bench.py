@@ -41,6 +41,7 @@ UNIT = "TFLOP/s"
 PREFILL_WL = wl.CONCURRENT_PREFILL_BATCH
 BEAM_WLS = (wl.LONG_PROMPT_WIDE_BEAM, wl.SHORT_PROMPT_BEAM)
 PREFILL_SEED = wl.workload_seed(3)
+STOP_ID = 151643
 
 
 def prefill_flops(lengths, n_q_heads, head_dim) -> float:
@@ -275,6 +276,102 @@ def run_decode_step(slm_lib, bs: BeamSet, t: int, stream_ptr):
         raise RuntimeError(slm_lib.slm_last_error().decode())
 
 
+def loop_bytes(bw) -> float:
+    """Algorithmic bytes of one fixed-depth loop: the first step's one logits
+    row, then per decode step the attention's bytes and the step's logits."""
+    b = select_bytes(1, bw.vocab)
+    for t in range(1, bw.steps + 1):
+        b += decode_attn_bytes(bw.beams, bw.prefix_len, t - 1, bw.n_q_heads, bw.n_kv_heads, bw.head_dim)
+        b += select_bytes(bw.beams, bw.vocab)
+    return float(b)
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2 between timed repetitions."""
+
+    def __init__(self, dev, nbytes: int = 256 << 20):
+        self.buf = torch.empty(nbytes // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def timed_reps(fn, stream, reps: int, warmup: int, flush=None):
+    """Median CUDA-event time (s) of fn() on `stream`, L2 flushed before each rep."""
+    for _ in range(warmup):
+        fn()
+    ms = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    return statistics.median(ms) / 1e3
+
+
+def measure_decode_loop(dev, bw, seed, stop_id, stream, peaks, flush, reps=20, warmup=3):
+    """The fixed-depth loop (first step + bw.steps decode steps) captured as
+    one CUDA graph: replay time, and the same loop enqueued call by call."""
+    from attention_packed_varlen_gb300.decode_loop import BeamDecodeLoop
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    W, Hq, Hkv, D, V = bw.beams, bw.n_q_heads, bw.n_kv_heads, bw.head_dim, bw.vocab
+    logits0 = device_randn((1, V), gen, dev, std=bw.logit_std)
+    kp = device_randn((bw.prefix_len, Hkv, D), gen, dev)
+    vp = device_randn((bw.prefix_len, Hkv, D), gen, dev)
+    steps = [(device_randn((W, Hq, D), gen, dev), device_randn((W, Hkv, D), gen, dev),
+              device_randn((W, Hkv, D), gen, dev), device_randn((W, V), gen, dev, std=bw.logit_std))
+             for _ in range(bw.steps)]
+    if stop_id is not None:  # a third of the rows rank the stop token first
+        for st in steps:
+            rows = torch.arange(0, W, 3, device=dev)
+            st[3][rows, stop_id] = (st[3][rows].float().amax(dim=1) + 0.5).to(torch.bfloat16)
+    loop = BeamDecodeLoop(W, V, bw.steps, bw.prefix_len, Hq, Hkv, D, stop_id=stop_id,
+                          softmax_scale=bw.softmax_scale, device=dev)
+    loop.capture(logits0, kp, vp, steps)
+    graph_s = timed_reps(loop.replay, stream, reps, warmup, flush)
+    eager_s = timed_reps(lambda: loop.record(logits0, kp, vp, steps), stream, reps, warmup, flush)
+    from attention_packed_varlen_gb300 import _binding as slm
+    slm.slm_check_status(loop.status)
+    n = bw.steps
+    launches = 4 + 1 + n * (1 + 4 + 1) + ((n + 1) if stop_id is not None else 0)
+    nbytes = loop_bytes(bw)
+    return {"stop_id": stop_id, "decode_steps": n, "graph_us_per_loop": graph_s * 1e6,
+            "graph_us_per_decode_step": graph_s * 1e6 / n, "eager_us_per_loop": eager_s * 1e6,
+            "launches_per_loop": launches, "bytes_per_loop": nbytes,
+            "hbm_frac_of_measured": nbytes / graph_s / 1e9 / peaks["hbm_gbs"]}
+
+
+def measure_heads(dev, stream, peaks, flush, T, reps=20, warmup=3):
+    """Fused SwiGLU + per-token E4M3 over the concurrent batch's token rows
+    (intermediate 5632), and last-token label scores of its 240 sequences."""
+    from attention_packed_varlen_gb300 import _binding as slm
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.workload_seed(6))
+    I = 5632
+    gu = device_randn((T, 2 * I), gen, dev, std=2.0)
+    s = timed_reps(lambda: slm.slm_swiglu_quant_e4m3(gu), stream, reps, warmup)
+    nbytes = float(T) * (2 * I * 2 + I + 4)
+    swiglu = {"tokens": T, "intermediate": I, "us": s * 1e6, "bytes": nbytes,
+              "achieved_gbs": nbytes / s / 1e9, "hbm_frac_of_measured": nbytes / s / 1e9 / peaks["hbm_gbs"],
+              "l2": "input 2x larger than L2 per call"}
+    del gu
+    lengths = wl.draw_lengths(PREFILL_WL.n_seqs, PREFILL_WL.len_lo, PREFILL_WL.len_hi, PREFILL_SEED)
+    cu = wl.cu_seqlens_from_lengths(lengths).to(dev)
+    d_model, n_labels = 2048, 8
+    hidden = device_randn((int(lengths.sum()), d_model), gen, dev)
+    w_label = device_randn((n_labels, d_model), gen, dev, std=0.05)
+    s = timed_reps(lambda: slm.slm_label_scores(hidden, cu, w_label), stream, reps, warmup, flush)
+    labels = {"sequences": len(lengths), "d_model": d_model, "n_labels": n_labels, "us": s * 1e6,
+              "bytes": float(len(lengths) * d_model * 2 + n_labels * d_model * 2),
+              "l2": "flushed before each call"}
+    return {"swiglu_e4m3": swiglu, "label_scores": labels}
+
+
 # ----------------------------------------------------------------------------
 # CPU oracle timing (bounded sample)
 # ----------------------------------------------------------------------------
@@ -487,13 +584,27 @@ def run_gpu(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "layers": args.e2e_layers}
 
+    # the fused fixed-depth loop (one CUDA graph) and the head kernels, timed
+    # after the main step with their own events
+    flush = L2Flush(dev)
+    decode_loop = {}
+    heads = None
+    if not args.no_extra_legs:
+        for j, bs in enumerate(beams):
+            bw = bs.w
+            decode_loop[bw.name] = {
+                "plain": measure_decode_loop(dev, bw, rank_beam_seed(bw, rank) + 1, None, stream, peaks, flush),
+                "with_stop_token": measure_decode_loop(dev, bw, rank_beam_seed(bw, rank) + 2, STOP_ID, stream,
+                                                       peaks, flush)}
+        heads = measure_heads(dev, stream, peaks, flush, ps.T)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tfl, cores, desc = oracle_prefill_sample(budget_s=args.ref_budget)
         cpu = {"value": tfl, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "cpu": cpu_model()}
 
-    # prefill: schedule + attention; decode step: attention + 3 selection kernels
-    launches_per_step = n_pre * 2 + sum(n_dec) * 4
+    # prefill: schedule + attention; decode step: attention + 4 selection kernels
+    launches_per_step = n_pre * 2 + sum(n_dec) * 5
     peak_sust = peaks["bf16_tflops_sustained"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -508,6 +619,8 @@ def run_gpu(args):
         },
         "prefill_pct_of_bf16_peak": {"sustained": value / world / peak_sust, "burst": value / world / peaks["bf16_tflops"]},
         "decode": decode,
+        "decode_loop_graph": decode_loop,
+        "heads": heads,
         "roofline": {"kernel": "slm_packed_prefill_attn (schedule + tcgen05 attention)", "bound": "tensor",
                      "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s", "frac": achieved / peak_sust,
                      "peak_kind": f"bf16 sustained, {peaks['source']}",
@@ -555,6 +668,8 @@ def main():
     ap.add_argument("--e2e-layers", type=int, default=28)
     ap.add_argument("--ref-budget", type=float, default=15.0, help="seconds of oracle work per sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-legs", action="store_true",
+                    help="skip the decode-loop graph and head-kernel timings")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per prefill launch from an ncu capture of the current kernel")
     ap.add_argument("--ncu-case", choices=["prefill", "decode"], default=None,

@@ -232,8 +232,9 @@ slm_status slm_beam_split_finished(const int32_t* cand_token, const int32_t* can
  *   hist_out int32 [W, max_len]: hist_out[b, s] = hist_in[parent[b], s] for
  *            s < t and hist_out[b, t] = token[b]; must not alias hist_in.
  *
- * A parent outside [0, W_in) reads row 0 and sets SLM_DEV_BAD_PARENT in
- * *dev_status (nullable).  Requires 0 <= t < max_len.
+ * When t > 0, a parent outside [0, W_in) reads row 0 and sets
+ * SLM_DEV_BAD_PARENT in *dev_status (nullable); at t = 0 no row is read and
+ * the parent index is ignored.  Requires 0 <= t < max_len.
  */
 slm_status slm_beam_reorder_history(const int32_t* hist_in, const int32_t* parent_idx, const int32_t* token,
                                     int32_t W, int32_t W_in, int32_t t, int32_t max_len, int32_t* hist_out,

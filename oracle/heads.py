@@ -161,3 +161,72 @@ def reorder_history(hist_in, parent, token, t: int):
             out[b, :t] = np.asarray(hist_in)[p, :t]
         out[b, t] = int(token[b])
     return out
+
+
+def beam_decode_loop(logits0, kp, vp, steps, W: int, softmax_scale: float, stop_id=None, follow=None,
+                     n_threads: int = 1):
+    """Fixed-depth beam search (section 2.3), one record per step.
+
+    Step 0 turns the prompt's last-row logits [1, V] into the first W beams
+    (cumulative score 0).  Decode step t = 1..len(steps) takes steps[t-1] =
+    (q [W,Hq,D], k_new, v_new [W,Hkv,D], logits [W,V]) of the beams chosen at
+    step t-1 and
+      1. attends over the shared prompt K/V plus each beam's suffix, the
+         suffix of step t-1 reordered by that step's parent index with the
+         new row appended (sections 3.2, 3.3);
+      2. ranks all W x V extensions by cumulative score and keeps the top 2W
+         candidates (section 3.3);
+      3. with a stop id, sets finished hypotheses aside (``split_finished``);
+      4. reorders the token history by the new parents (``reorder_history``).
+
+    Each record holds ``cand`` = (token, parent, score, lse) of the top 2W,
+    ``active`` = (token, parent, score) of the W beams that go on,
+    ``finished`` (list of (token, parent, score)), ``hist`` [W, t+1] and, for
+    t >= 1, the attention ``o``, ``lse`` and reordered suffix ``ks``/``vs``
+    (bf16 bits) of that step.
+
+    ``follow(t, rec)``, when given, returns the (token, parent, score) arrays
+    to go on with after step t instead of the record's own -- e.g. those of
+    another run whose near-equal scores were ordered differently -- so that
+    every later step is compared on the same beams.  The hypotheses ``hist``
+    and ``ks``/``vs`` follow the same beams."""
+    import oracle as _o  # the package's C-backed attention and selection
+
+    def split(tok, par, sc):
+        if stop_id is None:
+            return (tok[:W].astype(np.int32), par[:W].astype(np.int32), sc[:W].astype(np.float32)), []
+        act, fin = split_finished(tok, par, sc, W, stop_id)
+        return (np.array([a[0] for a in act], np.int32), np.array([a[1] for a in act], np.int32),
+                np.array([a[2] for a in act], np.float32)), fin
+
+    def go_on(t, rec):
+        if follow is None:
+            return rec["active"]
+        a = follow(t, rec)
+        return (np.asarray(a[0], np.int32), np.asarray(a[1], np.int32), np.asarray(a[2], np.float32))
+
+    recs = []
+    cand = _o.beam_select(logits0, np.zeros(1, np.float32), 2 * W)
+    active, fin = split(*cand[:3])
+    rec = {"cand": cand, "active": active, "finished": fin}
+    state = go_on(0, rec)
+    rec["hist"] = reorder_history(None, None, state[0], 0)
+    recs.append(rec)
+    hist = rec["hist"]
+    Hkv, D = np.asarray(_o._bits(kp)).shape[1:]
+    Smax = max(1, len(steps))
+    ks = np.zeros((W, Smax, Hkv, D), np.uint16)
+    vs = np.zeros_like(ks)
+    for t in range(1, len(steps) + 1):
+        q, k_new, v_new, logits = steps[t - 1]
+        parent = state[1]
+        o, lse, ks, vs = _o.shared_prefix_decode(q, kp, vp, ks, vs, k_new, v_new, parent, t - 1, softmax_scale,
+                                                 n_threads=n_threads)
+        cand = _o.beam_select(logits, state[2], 2 * W)
+        active, fin = split(*cand[:3])
+        rec = {"cand": cand, "active": active, "finished": fin, "o": o, "lse": lse, "ks": ks, "vs": vs}
+        state = go_on(t, rec)
+        hist = reorder_history(hist, state[1], state[0], t)
+        rec["hist"] = hist
+        recs.append(rec)
+    return recs

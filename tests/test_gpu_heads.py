@@ -141,3 +141,15 @@ def test_reorder_history_matches_oracle():
         slm.slm_beam_reorder_history(hist.to(DEV), parent.to(DEV), token.to(DEV), t, out)
         torch.cuda.synchronize()
         np.testing.assert_array_equal(out.cpu().numpy()[:, :t + 1], H.reorder_history(hist.numpy(), parent, token, t))
+
+
+def test_reorder_history_first_step_from_one_row():
+    # t = 0: the first beams' tokens, no parent rows (W_in = 1, identity parents ignored)
+    W = 100
+    token = torch.arange(W, dtype=torch.int32, device=DEV) * 7
+    out = torch.full((W, 5), -1, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slm.slm_beam_reorder_history(None, None, token, 0, out, dev_status=status)
+    slm.slm_check_status(status)
+    np.testing.assert_array_equal(out[:, 0].cpu().numpy(), token.cpu().numpy())
+    assert (out[:, 1:].cpu() == -1).all()
