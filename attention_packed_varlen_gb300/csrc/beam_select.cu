@@ -1,43 +1,43 @@
 // Two-stage beam candidate selection on sm_103a (article "SLM 生成式高并发推理引擎：
 // 延迟约束下的有效吞吐优化", section 3.3):
 //
-//   BF16 logits [W_in, V] -> per beam the 2W largest logits (token ids; lowest
-//   id on equal logits) -> scores read from the FP32 log-softmax over the full
-//   vocabulary, plus the beam's cumulative score -> flatten W_in x 2W -> the
-//   global 2W best (higher score first; equal scores by lower parent, then
-//   higher logit, then lower id) with parents.
+//   BF16 logits [W_in, V] -> scores read from the FP32 log-softmax over the
+//   full vocabulary plus the beam's cumulative score -> the global 2W best
+//   (higher score first; equal scores by lower parent, then higher logit,
+//   then lower id) with their parents.
 //
-// The article's pruning claim (a token below rank 2W in its own beam cannot
-// reach the global top 2W) is used the other way round: every beam hands the
-// global stage a superset of its top 2W -- all of its logits at or above a
-// threshold tau_b -- and the global stage ranks that superset with the full
-// order.  The result is the same, and no per-beam sort is needed.
+// The article's pruning claim -- a candidate outside the best few of its own
+// group cannot reach the global 2W -- is applied to groups of logits smaller
+// than a beam: tiles of 8192 consecutive logits of one row, and within a tile
+// 128 interleaved groups of 64 ("sub-chunks").  A group's best score is that
+// of its largest logit (the score is monotone in the logit), and 2W distinct
+// groups' best scores are 2W real candidates, so the 2W-th largest group
+// maximum L is at most the global 2W-th score: every global candidate lies in
+// a group whose maximum scores >= L, and is itself >= L.  Only those groups
+// are read again, and only their logits scoring >= L are ranked.
 //
-// Four kernels, one read of the logits from HBM; each later kernel is
-// launched as a programmatic dependent of the one before, so it is resident
-// and waiting (griddepcontrol.wait) when its predecessor ends:
+// Three kernels, the logits read once from HBM plus a few hundred small groups:
 //
-// 1. prep (one CTA per beam): resets the per-call counters and the score
-//    histogram, and from 4096 sampled logits picks tau_b (keeps the beam's 2W
-//    best with near certainty while passing ~1.5% of the row) and a softmax
-//    reference R_b (the sample maximum).
-// 2. stream (persistent, one CTA per SM): a producer warp streams 16 KB tiles
-//    of the logits into an 8-stage shared-memory ring with 1-D bulk copies
-//    (cp.async.bulk) completing on mbarriers, issuing its first copies while
-//    prep still runs; eight consumer warps each take 1/8 of a tile: the
-//    partial sum of exp(x - R_b) on packed f32x2 FMAs and ex2, the maximum,
-//    and the logits >= tau_b, appended to the beam's candidate list.  Nothing
-//    in the loop waits on another CTA.
-// 3. finish (one CTA per beam): lse_b from the partials, and the candidates'
-//    scores histogrammed (upper 16 bits of an order-preserving key) into a
-//    global histogram.  A beam whose threshold missed (too few or too many
-//    candidates) is first redone exactly from its row.
-// 4. final: every CTA reads from the histogram the bin B* that holds the
-//    global 2W-th best score, the CTAs copy their beams' candidates in bins
-//    >= B* to a small list, and the last CTA to finish sorts that list
-//    (bitonic, in shared memory) with the full order and writes the 2W
-//    results.  A list that would overflow (huge score ties) is resolved by an
-//    exact radix select over all candidates instead.
+// 1. stream (persistent, one CTA per SM): a producer warp streams 16 KB tiles
+//    into a 12-stage shared-memory ring with 1-D bulk copies (cp.async.bulk)
+//    completing on mbarriers; twelve consumer warps, one per ring slot, take
+//    whole tiles: the maximum of each of the tile's 128 sub-chunks (packed
+//    bf16x2 max), then the tile's sum of exp(x - M_t) relative to its
+//    maximum (packed f32x2 FMA and ex2).  Per tile it writes (M_t, sum) and the 128 sub-chunk maxima.
+// 2. row statistics (a warp per beam, or a CTA per beam when the groups are
+//    sub-chunks; a programmatic dependent of the stream): lse_b from the
+//    beam's tile partials in a fixed order, each group's best score key, and
+//    a histogram of the keys' upper 16 bits with their maximum.
+// 3. select (one CTA per SM, a programmatic dependent of the row kernel):
+//    every CTA walks the histogram down to the bin holding the 2W-th largest
+//    group key -- its lower edge is L, at most that key -- lists the groups
+//    scoring >= L in group order, and takes its share of them: it reads
+//    their sub-chunks scoring >= L back from the logits and appends the
+//    logits scoring >= L to a small list.  The last CTA to finish ranks that
+//    list with the full order (score bins, then pairwise within a bin) and
+//    writes the 2W results.  If the list would overflow (huge score ties)
+//    the last CTA ranks every logit scoring >= L exactly with a radix select
+//    instead.
 //
 // Every wait on an mbarrier is bounded; a wait that runs out marks the call
 // failed and the outputs are filled with -1 ids and NaN scores.
@@ -55,32 +55,38 @@ namespace slm {
 namespace sel {
 
 constexpr int kTile = 8192;                        // logits per streamed tile (16 KB)
-constexpr int kCWarps = 8;                         // consumer warps of the stream kernel
+constexpr int kCWarps = 12;                        // consumer warps of the stream kernel
 constexpr int kVec = 4;                            // 16-byte vectors per lane and chunk
 constexpr int kChunkElems = kVec * 8 * 32;         // 1024 logits per chunk
 constexpr int kChunks = kTile / kChunkElems;       // 8 chunks per tile
 constexpr int kStages = 12;                        // ring depth (192 KB)
-constexpr int kSegCap = 256;                       // candidate slots per tile (rows longer than a tile)
 constexpr int kStreamThreads = 32 * (kCWarps + 1);
-constexpr int kCap = 8192;                         // candidates per beam
-constexpr int kLocalBins = 1024;                   // per-beam score histogram in shared memory
-constexpr int kMaxTiles = (1 << 24) / kTile;       // tiles per row at the largest vocabulary
-constexpr int kFineBins = 65536;                   // global score histogram (key >> 16)
-constexpr int kEliteMax = 4096;                    // entries the final ranking holds, at most
-constexpr int kPrepThreads = 256;
-constexpr int kSamples = 4096;
-constexpr int kFinalThreads = 256;
-constexpr int kFinalWarps = kFinalThreads / 32;
+constexpr int kQuarters = 4;                       // sub-chunks per lane and tile (2 chunks each)
+constexpr int kSubPerTile = kQuarters * 32;        // 128 sub-chunks of 64 logits per tile
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kRowThreads = 256;                   // row-statistics kernel: a warp per beam
+constexpr int kRowWarps = kRowThreads / 32;
+constexpr int kMaxRows = 1024;                     // W_in limit
+constexpr int kUnitCap = 8192;                     // groups the normal path lists
+constexpr int kCandCap = 4096;                     // candidates the final sort holds
 constexpr float kLog2e = 1.4426950408889634f;
-static_assert(kCap >= kTile, "a one-tile row must fit the candidate list whole");
 constexpr uint32_t kNegInf2 = 0xFF80FF80u;         // two bf16 -inf
 constexpr unsigned kFull = 0xffffffffu;
+static_assert(kChunks % kQuarters == 0, "a sub-chunk is a whole number of chunks");
+// Consumer warp w takes the CTA's tiles w, w + kCWarps, ...; with kStages a
+// multiple of kCWarps every ring slot is read by one warp only, so a warp
+// waiting on a slot's "full" barrier is never two phases ahead of it (where
+// the parity of the phase it wants would match an older, completed phase).
+static_assert(kStages % kCWarps == 0, "each ring slot has a single consumer warp");
 
 // misc words of the workspace
-constexpr int kMiscElite = 0;    // entries appended to the final list
-constexpr int kMiscTicket = 1;   // final-kernel CTAs done
-constexpr int kMiscMaxKey = 2;   // largest candidate score key
-constexpr int kMiscStatus = 3;   // nonzero: a bounded wait ran out or the histogram was inconsistent
+constexpr int kMiscCand = 0;     // candidates appended
+constexpr int kMiscTicket = 1;   // select-kernel CTAs done
+constexpr int kMiscStatus = 2;   // nonzero: a bounded wait ran out
+constexpr int kMiscMaxKey = 3;   // largest group key
+constexpr int kMiscWords = 4;
+constexpr int kHistBins = 65536; // group keys >> 16
 
 // ---------------------------------------------------------------------------
 // Order-preserving keys
@@ -281,20 +287,15 @@ struct Params {
   const float* cum;        // [W_in]
   int W_in, V, K, W;       // K = 2W candidates kept globally
   int n_tpr, n_tiles;      // tiles per row, tiles in all
-  int seg_cap;             // candidate slots per tile
   bool vec_ok;             // rows 16-byte aligned: bulk copies and vector loads
   // workspace
-  float* tau;                  // [W_in] candidate threshold
-  float* ref;                  // [W_in] softmax reference R_b
-  float* lse;                  // [W_in]
-  int* cand_count;             // [W_in] entries of cand
-  unsigned long long* seg;     // [W_in, n_tpr, seg_cap] candidates as the stream finds them
-  float4* partial;             // [W_in, n_tpr] (reference, sum of exp, max logit, candidates as int bits)
-  unsigned long long* cand;    // [W_in, kCap] each beam's candidates, contiguous
-  unsigned* fine;              // [kFineBins]
-  unsigned* misc;              // [4]
-  ulonglong2* elite;           // [elite_cap]
-  int elite_cap;
+  float2* partial;         // [n_tiles] (tile maximum M_t, sum of exp(x - M_t))
+  uint16_t* submax;        // [n_tiles, kSubPerTile] sub-chunk maxima (bf16 bits)
+  float* lse;              // [W_in]
+  uint32_t* gkeys;         // [groups] each group's best score key
+  unsigned* hist;          // [kHistBins] group keys by their upper 16 bits
+  ulonglong2* cand;        // [kCandCap] candidates in the global order encoding
+  unsigned* misc;          // [kMiscWords]
   // outputs
   int32_t* out_token;
   int32_t* out_parent;
@@ -305,106 +306,17 @@ struct Params {
   float* out_lse;
 };
 
-// ---------------------------------------------------------------------------
-// 1. prep
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const Params p) {
-  grid_dep_launch();
-  constexpr int kPerThread = kSamples / kPrepThreads;  // 16 sampled logits per thread
-  static_assert(kPrepThreads == 256, "one histogram bin per thread");
-  __shared__ unsigned hist[256];
-  __shared__ unsigned wmaxk[kPrepThreads / 32];
-  __shared__ int tau_key, found;
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-
-  if (b == 0 && tid < 4) p.misc[tid] = 0;
-  {
-    const int n4 = kFineBins / 4;
-    const int per = (n4 + gridDim.x - 1) / gridDim.x;
-    uint4* f4 = reinterpret_cast<uint4*>(p.fine);
-    const int end = min(n4, (b + 1) * per);
-    for (int i = b * per + tid; i < end; i += kPrepThreads) f4[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
-
-  // 4096 sampled logits as order-preserving 16-bit keys
-  const uint16_t* row = p.logits + static_cast<int64_t>(b) * p.V;
-  uint32_t key[kPerThread];
-  if (p.vec_ok) {
-    // 512 runs of 8 logits (16 bytes) at evenly spaced, 8-aligned offsets
-    constexpr int kRuns = kSamples / 8;
-#pragma unroll
-    for (int k = 0; k < kPerThread / 8; ++k) {
-      const int j = tid + k * kPrepThreads;
-      const int64_t off = (static_cast<int64_t>(j) * (p.V - 8) / (kRuns - 1)) & ~int64_t(7);
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + off));
-      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        key[8 * k + 2 * h] = bf16_key(wd[h] & 0xFFFFu);
-        key[8 * k + 2 * h + 1] = bf16_key(wd[h] >> 16);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-      const int s_ = tid + k * kPrepThreads;
-      key[k] = bf16_key(row[static_cast<int64_t>(s_) * (p.V - 1) / (kSamples - 1)]);
-    }
-  }
-  uint32_t mk = 0;
-#pragma unroll
-  for (int k = 0; k < kPerThread; ++k) mk = max(mk, key[k]);
-  mk = warp_max_u32(mk);
-  if (lane == 0) wmaxk[w] = mk;
-  __syncthreads();
-  uint32_t M = wmaxk[0];
-  for (int i = 1; i < kPrepThreads / 32; ++i) M = max(M, wmaxk[i]);
-  if (tid == 0) p.ref[b] = bf16_bits_to_f32(key_to_bf16(M));
-  if (p.V <= kCap) {  // the whole row fits the candidate list
-    if (tid == 0) p.tau[b] = -INFINITY;
-    return;
-  }
-  // tau_b: the r-th largest sample, r a few standard deviations above the
-  // expected sample count of the beam's K best.  The keys just below the
-  // maximum are histogrammed (256 bins); a window too narrow to hold r
-  // samples is widened 16-fold.
-  const float expect = static_cast<float>(p.K) * kSamples / p.V;
-  const int r = min(kSamples, static_cast<int>(ceilf(expect + 6.f * sqrtf(expect) + 8.f)));
-  for (int sh = 0; sh <= 8; sh += 4) {
-    hist[tid] = 0u;  // kPrepThreads == 256 bins
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kPerThread; ++k) {
-      const uint32_t d = (M - key[k]) >> sh;
-      if (d < 256u) atomicAdd(&hist[255u - d], 1u);
-    }
-    __syncthreads();
-    if (w == 0) {
-      int in_window = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) in_window += static_cast<int>(hist[8 * lane + i]);
-      in_window = __shfl_sync(kFull, warp_inclusive_scan(in_window, lane), 31);
-      int digit = 0, above, in_bin;
-      if (in_window >= r) warp_pick(hist, r, lane, &digit, &above, &in_bin);
-      // bin 255 - d holds the keys with (M - key) >> sh == d
-      if (lane == 0) {
-        found = (in_window >= r);
-        tau_key = static_cast<int>(M) - ((255 - digit + 1) << sh) + 1;
-      }
-    }
-    __syncthreads();
-    if (found || sh == 8) break;
-    __syncthreads();
-  }
-  if (tid == 0) {
-    // keys below that of -inf (NaN patterns) clamp to -inf
-    const uint32_t k = static_cast<uint32_t>(max(tau_key, static_cast<int>(bf16_key(0xFF80u))));
-    p.tau[b] = bf16_bits_to_f32(key_to_bf16(k));
-  }
+// Tile-relative position of logit e (0..7) of run r (0..7) of sub-chunk (q, l):
+// the lane l of a consumer warp reads, in chunk ch and vector v, the logits
+// ch * 1024 + (v * 32 + l) * 8 + 0..7; sub-chunk (q, l) is what lane l reads in
+// chunks 2q and 2q + 1.
+__device__ __forceinline__ int sub_run_offset(int q, int l, int r) {
+  const int ch = q * (kChunks / kQuarters) + (r >> 2), v = r & 3;
+  return ch * kChunkElems + (v * 32 + l) * 8;
 }
 
 // ---------------------------------------------------------------------------
-// 2. stream
+// 1. stream
 // ---------------------------------------------------------------------------
 struct StreamSmem {
   uint4 ring[kStages][kTile / 8];
@@ -463,127 +375,85 @@ __device__ __forceinline__ void chunk_exp_sum(const uint4 (&r)[kVec], float cc, 
 }
 
 // Loads chunk ch of a ring slot: vector v of the lane holds tile logits
-// (ch * 1024 + (v * 32 + lane) * 8) + 0..7; vectors past the tile's n logits
-// read as -inf.
+// (ch * 1024 + (v * 32 + lane) * 8) + 0..7.  With full = false, vectors past
+// the tile's n logits read as -inf.
+template <bool kFullTile>
 __device__ __forceinline__ void load_chunk(const uint4* slot, int ch, int lane, int n, uint4 (&r)[kVec]) {
 #pragma unroll
   for (int v = 0; v < kVec; ++v) {
     const int e0 = ch * kChunkElems + (v * 32 + lane) * 8;
-    r[v] = (e0 < n) ? slot[ch * (kChunkElems / 8) + v * 32 + lane]
-                    : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+    r[v] = (kFullTile || e0 < n) ? slot[ch * (kChunkElems / 8) + v * 32 + lane]
+                                 : make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
   }
 }
 
-// Consumer warp cw takes the CTA's tiles cw, cw + 8, cw + 16, ... whole, so
-// the warps work on different tiles and no warp waits for another.  Per
-// chunk of 1024 logits a lane holds 32: it adds their exp(x - R_b) to its
-// sums and marks those >= tau_b in a 32-bit mask (bit 4v + h for the low
-// logit of word h of vector v, bit 16 + 4v + h for the high one).  After the
-// tile one warp scan places the marked logits in the tile's candidate
-// segment; they are read back from the ring slot, which is released only then.
-__device__ void stream_consumer(const Params& p, StreamSmem& sh, int cw, int lane) {
-  grid_dep_wait();  // tau, ref and the reset counters come from the prep kernel
-  const int step = kCWarps * gridDim.x;
-  int t = blockIdx.x + cw * gridDim.x;
-  float tau_n = 0.f, ref_n = 0.f;
-  if (t < p.n_tiles) {
-    tau_n = __ldcg(p.tau + t / p.n_tpr);
-    ref_n = __ldcg(p.ref + t / p.n_tpr);
+__device__ __forceinline__ uint32_t hmax2_u32(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// The larger of the two bf16 halves, as bf16 bits.
+__device__ __forceinline__ uint32_t hmax_halves(uint32_t a) {
+  return hmax2_u32(a, (a >> 16) | (a << 16)) & 0xFFFFu;
+}
+
+// One tile in a consumer warp: the 128 sub-chunk maxima (lane l holds
+// sub-chunks (q, l), q = 0..3), the tile maximum, and the sum of exp(x - M).
+template <bool kFullTile>
+__device__ __forceinline__ void consume_tile(const uint4* slot, int n, int lane, uint32_t (&qb)[kQuarters],
+                                             float& M, float& l_sum) {
+  float lm = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kQuarters; ++q) {
+    uint32_t qm = kNegInf2;
+#pragma unroll
+    for (int k = 0; k < kChunks / kQuarters; ++k) {
+      uint4 r[kVec];
+      load_chunk<kFullTile>(slot, q * (kChunks / kQuarters) + k, lane, n, r);
+#pragma unroll
+      for (int v = 0; v < kVec; ++v)
+        qm = hmax2_u32(hmax2_u32(qm, r[v].x), hmax2_u32(hmax2_u32(r[v].y, r[v].z), r[v].w));
+    }
+    qb[q] = hmax_halves(qm);
+    lm = fmaxf(lm, bf16_bits_to_f32(qb[q]));
   }
-  for (int i = cw; t < p.n_tiles; i += kCWarps, t += step) {
+  M = warp_max(lm);
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  if (M > -INFINITY) {
+    const float cc = -M * kLog2e;
+#pragma unroll 2
+    for (int ch = 0; ch < kChunks; ++ch) {
+      uint4 r[kVec];
+      load_chunk<kFullTile>(slot, ch, lane, n, r);
+      chunk_exp_sum(r, cc, s0, s1, s2, s3);
+    }
+  }
+  l_sum = (s0 + s1) + (s2 + s3);
+}
+
+// Consumer warp cw takes the CTA's tiles cw, cw + kCWarps, ... whole, so the
+// warps work on different tiles and no warp waits for another; each ring slot
+// belongs to one warp.
+__device__ void stream_consumer(const Params& p, StreamSmem& sh, int cw, int lane) {
+  const int step = kCWarps * gridDim.x;
+  for (int i = cw, t = blockIdx.x + cw * gridDim.x; t < p.n_tiles; i += kCWarps, t += step) {
     const int s = i % kStages;
     const int b = t / p.n_tpr, c = t - b * p.n_tpr;
     const int n = min(kTile, p.V - c * kTile);
-    const float tau = tau_n, R0 = ref_n;
-    if (t + step < p.n_tiles) {  // the next tile's beam values, early
-      tau_n = __ldcg(p.tau + (t + step) / p.n_tpr);
-      ref_n = __ldcg(p.ref + (t + step) / p.n_tpr);
-    }
     const bool ok = mbar_wait(&sh.full[s], (i / kStages) & 1, &sh.abort);
     if (!__all_sync(kFull, ok)) break;
-
     const uint4* slot = &sh.ring[s][0];
-    const bool keep_all = !(tau > -INFINITY);  // rows of one tile: every logit is a candidate
-    const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);  // tau is a bf16 value or -inf
-    const float mref = (R0 > -INFINITY) ? R0 : 0.f;
-    const float cc = -mref * kLog2e;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-    uint32_t cb[kChunks];
-#pragma unroll
-    for (int ch = 0; ch < kChunks; ++ch) {
-      uint4 r[kVec];
-      load_chunk(slot, ch, lane, n, r);
-      chunk_exp_sum(r, cc, s0, s1, s2, s3);
-      uint32_t bits = 0u;
-#pragma unroll
-      for (int v = 0; v < kVec; ++v) {
-        const uint32_t wd[4] = {r[v].x, r[v].y, r[v].z, r[v].w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-          bits |= __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&wd[h]), t2) & (0x00010001u << (4 * v + h));
-      }
-      if (keep_all) {  // -inf padding past the tile's end must not count
-#pragma unroll
-        for (int v = 0; v < kVec; ++v) {
-          const int nv = min(max(n - (ch * kChunkElems + (v * 32 + lane) * 8), 0), 8);
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            if (2 * h >= nv) bits &= ~(1u << (4 * v + h));
-            if (2 * h + 1 >= nv) bits &= ~(1u << (16 + 4 * v + h));
-          }
-        }
-      }
-      cb[ch] = bits;
-    }
-
-    // candidates to the tile's segment, in lane order
-    int cnt = 0;
-#pragma unroll
-    for (int ch = 0; ch < kChunks; ++ch) cnt += __popc(cb[ch]);
-    const int incl = warp_inclusive_scan(cnt, lane);
-    const int found = __shfl_sync(kFull, incl, 31);
-    int pos = incl - cnt;
-    unsigned long long* seg = p.seg + (static_cast<int64_t>(b) * p.n_tpr + c) * p.seg_cap;
-    const uint16_t* slot16 = reinterpret_cast<const uint16_t*>(slot);
-    float cmax = -INFINITY;  // largest candidate of the lane
-#pragma unroll
-    for (int ch = 0; ch < kChunks; ++ch) {
-      uint32_t bits = cb[ch];
-      while (bits) {
-        const int j = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        const int q = j & 15;
-        const int e = ch * kChunkElems + ((q >> 2) * 32 + lane) * 8 + 2 * (q & 3) + (j >> 4);
-        const uint32_t xb = slot16[e];
-        cmax = fmaxf(cmax, bf16_bits_to_f32(xb));
-        if (pos < p.seg_cap) seg[pos] = cand_entry(xb, static_cast<uint32_t>(c * kTile + e));
-        ++pos;
-      }
-    }
-    // A candidate far above the reference (possible only when the sample
-    // missed the row's top) overflowed exp: this lane's sum is redone against
-    // its own maximum.
-    float m_l = mref;
-    if (cmax - mref > 64.f) {
-      m_l = cmax;
-      s0 = s1 = s2 = s3 = 0.f;
-#pragma unroll 1
-      for (int ch = 0; ch < kChunks; ++ch) {
-        uint4 r[kVec];
-        load_chunk(slot, ch, lane, n, r);
-        chunk_exp_sum(r, -m_l * kLog2e, s0, s1, s2, s3);
-      }
-    }
+    uint32_t qb[kQuarters];
+    float M, l;
+    if (n == kTile) consume_tile<true>(slot, n, lane, qb, M, l);
+    else consume_tile<false>(slot, n, lane, qb, M, l);
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);  // the slot's data is no longer read
-
-    // the tile's partial: common reference, sum, largest candidate, count
-    const float M = warp_max(m_l);
-    float l = (s0 + s1) + (s2 + s3);
-    if (m_l != M) l *= ex2((m_l - M) * kLog2e);
     l = warp_sum(l);
-    const float wm = warp_max(cmax);
-    if (lane == 0) p.partial[static_cast<int64_t>(b) * p.n_tpr + c] = make_float4(M, l, wm, __int_as_float(found));
+    if (lane == 0) p.partial[t] = make_float2(M, l);
+    uint16_t* sm = p.submax + static_cast<int64_t>(t) * kSubPerTile;
+#pragma unroll
+    for (int q = 0; q < kQuarters; ++q) sm[q * 32 + lane] = static_cast<uint16_t>(qb[q]);
   }
 }
 
@@ -598,6 +468,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     }
     sh.abort = 0;
     fence_mbarrier_init();
+    if (blockIdx.x == 0)
+      for (int i = 0; i < kMiscWords; ++i) p.misc[i] = 0u;  // read by the select kernel after this grid ends
+  }
+  {  // this CTA's slice of the group-key histogram (filled by the row kernel after this grid ends)
+    const int per = (kHistBins + gridDim.x - 1) / gridDim.x;
+    const int end = min(kHistBins, (static_cast<int>(blockIdx.x) + 1) * per);
+    for (int i = blockIdx.x * per + threadIdx.x; i < end; i += kStreamThreads) p.hist[i] = 0u;
   }
   __syncthreads();
   grid_dep_launch();
@@ -608,49 +485,16 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
 }
 
 // ---------------------------------------------------------------------------
-// Block primitives of the finish and final kernels (kBlockThreads threads)
+// Block primitives of the select kernel (kSelThreads threads)
 // ---------------------------------------------------------------------------
 struct Scratch {
-  unsigned whist[kFinalWarps][256];
   unsigned hist[256];
-  unsigned lbins[kLocalBins];
-  unsigned long long wu64[2][kFinalWarps];
-  float wf[kFinalWarps];
-  int wint[kFinalWarps];
-  int digit, above, in_bin, counter, flag, bstar, bstar_above, bstar_count;
+  unsigned long long wu64[2][kSelWarps];
+  int wint[kSelWarps];
+  uint32_t wkey[kSelWarps];
+  int digit, above, in_bin, counter, flag, dstar;
   unsigned long long u64;
 };
-
-__device__ __forceinline__ float block_max(float v, Scratch& sh) {
-  v = warp_max(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.wf[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = sh.wf[0];
-  for (int i = 1; i < kFinalWarps; ++i) r = fmaxf(r, sh.wf[i]);
-  return r;
-}
-
-__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Scratch& sh) {
-  v = warp_max_u32(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.wint[threadIdx.x >> 5] = static_cast<int>(v);
-  __syncthreads();
-  uint32_t r = 0;
-  for (int i = 0; i < kFinalWarps; ++i) r = max(r, static_cast<uint32_t>(sh.wint[i]));
-  return r;
-}
-
-// Sum in a fixed order (deterministic).
-__device__ __forceinline__ float block_sum(float v, Scratch& sh) {
-  v = warp_sum(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.wf[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = 0.f;
-  for (int i = 0; i < kFinalWarps; ++i) r += sh.wf[i];
-  return r;
-}
 
 __device__ __forceinline__ int block_scan_excl(int v, int* total, Scratch& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -659,7 +503,7 @@ __device__ __forceinline__ int block_scan_excl(int v, int* total, Scratch& sh) {
   if (lane == 31) sh.wint[w] = x;
   __syncthreads();
   int base = 0, tot = 0;
-  for (int i = 0; i < kFinalWarps; ++i) {
+  for (int i = 0; i < kSelWarps; ++i) {
     if (i < w) base += sh.wint[i];
     tot += sh.wint[i];
   }
@@ -667,12 +511,22 @@ __device__ __forceinline__ int block_scan_excl(int v, int* total, Scratch& sh) {
   return base + x - v;
 }
 
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Scratch& sh) {
+  v = warp_max_u32(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh.wkey[threadIdx.x >> 5] = v;
+  __syncthreads();
+  uint32_t r = 0;
+  for (int i = 0; i < kSelWarps; ++i) r = max(r, sh.wkey[i]);
+  return r;
+}
+
 // k-th largest (1-based, counting repeats) of the 64-bit keys all threads
 // visit with for_each(f).  Each pass histograms the keys in the live range
 // [lo, hi] by the 8 bits below the range's leading bit and narrows the range
 // to the bin holding the k-th key; a bin with a single key ends it.
 template <class ForEach>
-__device__ unsigned long long block_kth(ForEach for_each, int k, Scratch& sh) {
+__device__ unsigned long long block_kth(ForEach for_each, int k, Scratch& sh, unsigned (*whist)[256]) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   unsigned long long lo = ~0ull, hi = 0ull;
   for_each([&](unsigned long long key) {
@@ -689,22 +543,22 @@ __device__ unsigned long long block_kth(ForEach for_each, int k, Scratch& sh) {
   __syncthreads();
   lo = ~0ull;
   hi = 0ull;
-  for (int i = 0; i < kFinalWarps; ++i) {
+  for (int i = 0; i < kSelWarps; ++i) {
     lo = min(lo, sh.wu64[0][i]);
     hi = max(hi, sh.wu64[1][i]);
   }
   while (lo < hi) {
     const int sft = max(0, 64 - __clzll(hi - lo) - 8);
-    for (int i = threadIdx.x; i < kFinalWarps * 256; i += kFinalThreads) (&sh.whist[0][0])[i] = 0u;
+    for (int i = threadIdx.x; i < kSelWarps * 256; i += kSelThreads) (&whist[0][0])[i] = 0u;
     __syncthreads();
     const unsigned long long lo_c = lo, hi_c = hi;
     for_each([&](unsigned long long key) {
-      if (key >= lo_c && key <= hi_c) atomicAdd(&sh.whist[w][static_cast<uint32_t>((key - lo_c) >> sft)], 1u);
+      if (key >= lo_c && key <= hi_c) atomicAdd(&whist[w][static_cast<uint32_t>((key - lo_c) >> sft)], 1u);
     });
     __syncthreads();
-    {
+    if (threadIdx.x < 256) {
       unsigned s = 0;
-      for (int i = 0; i < kFinalWarps; ++i) s += sh.whist[i][threadIdx.x];  // kFinalThreads == 256
+      for (int i = 0; i < kSelWarps; ++i) s += whist[i][threadIdx.x];
       sh.hist[threadIdx.x] = s;
     }
     __syncthreads();
@@ -739,12 +593,12 @@ __device__ unsigned long long block_kth(ForEach for_each, int k, Scratch& sh) {
   return lo;
 }
 
-// Descending bitonic sort of ent[0, n_pow2).
+// Descending bitonic sort of ent[0, n_pow2) (the rare exact path only).
 __device__ void block_sort_desc(ulonglong2* ent, int n_pow2) {
   for (int size = 2; size <= n_pow2; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       __syncthreads();
-      for (int t = threadIdx.x; t < n_pow2 / 2; t += kFinalThreads) {
+      for (int t = threadIdx.x; t < n_pow2 / 2; t += kSelThreads) {
         const int lo = 2 * t - (t & (stride - 1));
         const int hi = lo + stride;
         const bool desc = ((lo & size) == 0);
@@ -766,299 +620,297 @@ __device__ __forceinline__ int next_pow2(int x) {
 }
 
 // ---------------------------------------------------------------------------
-// 3. finish (one CTA per beam)
+// 2. row statistics (a warp per beam)
 // ---------------------------------------------------------------------------
-// The threshold missed for beam b (too few logits above it, or more than the
-// list holds): the beam's exact top K from its whole row replaces the list.
-__device__ void exact_beam(const Params& p, Scratch& sh, int b) {
-  const uint16_t* row = p.logits + static_cast<int64_t>(b) * p.V;
-  const int V = p.V;
-  auto for_each = [&](auto f) {
-    for (int j = threadIdx.x; j < V; j += kFinalThreads) f(local_key(bf16_key(row[j]), static_cast<uint32_t>(j)));
-  };
-  const unsigned long long kth = block_kth(for_each, p.K, sh);
-  if (threadIdx.x == 0) sh.counter = 0;
-  __syncthreads();
-  unsigned long long* dst = p.cand + static_cast<int64_t>(b) * kCap;
-  for (int j = threadIdx.x; j < V; j += kFinalThreads) {
-    const uint32_t bits = row[j];
-    if (local_key(bf16_key(bits), static_cast<uint32_t>(j)) >= kth) {
-      const int pos = atomicAdd(&sh.counter, 1);
-      if (pos < kCap) dst[pos] = cand_entry(bits, static_cast<uint32_t>(j));
-    }
-  }
-  __threadfence();  // the list is read back below from L2
-  __syncthreads();
-  if (threadIdx.x == 0) p.cand_count[b] = p.K;
+// Score key fl32(cum + fl32(x - lse)), order-preserving.
+__device__ __forceinline__ uint32_t score_key_x(float x, float cum, float lse) {
+  return f32_key(__fadd_rn(cum, __fsub_rn(x, lse)));
 }
 
-// Beam b: lse_b from the stream partials; the tiles' candidate segments
-// gathered into one list; the candidates' scores into the global histogram
-// and the largest score key into misc.
-//
-// Rows of up to 32 tiles (vocabularies up to 262,144) take a path without
-// block-wide steps before the histogram: every warp reads all of the beam's
-// partials (lse_b and the segment offsets come out of warp reductions, the
-// same in every warp), finds the tile of each list entry it moves by a
-// binary search over the lanes, and requests eight entries per thread at once.
-constexpr int kFastTiles = 32;
+// lse_b from the beam's tiles (fixed order: lane j holds tile j, then the
+// warp's butterfly reductions), then the key of every group of the beam --
+// its tiles when there are at least K tiles in all, else its sub-chunks --
+// into gkeys, the histogram of the keys' upper 16 bits, and the largest key.
+// One red.add per distinct histogram bin among the warp's lanes.
+__device__ __forceinline__ void hist_add(unsigned* hist, uint32_t key, bool valid) {
+  const uint32_t bin = valid ? (key >> 16) : 0xFFFFFFFFu;
+  const unsigned peers = __match_any_sync(kFull, bin);
+  if (valid && (threadIdx.x & 31) == static_cast<unsigned>(__ffs(peers) - 1)) red_add(hist + bin, __popc(peers));
+}
 
-__global__ void __launch_bounds__(kFinalThreads) finish_kernel(const Params p) {
-  __shared__ Scratch sh;
-  __shared__ int start[kMaxTiles + 1];  // first list entry of each tile's segment
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-  uint32_t kmax = 0;  // largest score key this thread histograms
-  for (int d = tid; d < kLocalBins; d += kFinalThreads) sh.lbins[d] = 0u;
-  __syncthreads();
+__global__ void __launch_bounds__(kRowThreads) rowstat_kernel(const Params p) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool sub_level = p.n_tiles < p.K;
+  // tile groups: a warp per beam; sub-chunk groups: a CTA per beam
+  const int b = sub_level ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) * kRowWarps + warp;
   grid_dep_wait();
   grid_dep_launch();
+  if (b >= p.W_in) return;
   const int nt = p.n_tpr;
-  const float4* P = p.partial + static_cast<int64_t>(b) * nt;
-  const unsigned long long* seg = p.seg + static_cast<int64_t>(b) * nt * p.seg_cap;
-  unsigned long long* cand = p.cand + static_cast<int64_t>(b) * kCap;
+  const float2* P = p.partial + static_cast<int64_t>(b) * nt;
   const float cum = __ldg(p.cum + b);
-
-  float lse, top;
-  int count;
-  bool over;
-  if (nt <= kFastTiles) {
-    const float4 q = (lane < nt) ? __ldcg(P + lane) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-    const float M = warp_max(q.y > 0.f ? q.x : -INFINITY);
-    top = warp_max(q.z);
-    const float L = warp_sum(q.y > 0.f ? q.y * ex2((q.x - M) * kLog2e) : 0.f);
-    lse = M + logf(L);
-    const int cnt = (lane < nt) ? __float_as_int(q.w) : 0;
-    over = __any_sync(kFull, cnt > p.seg_cap);
-    const int incl = warp_inclusive_scan(cnt, lane);
-    const int st = incl - cnt;  // lane j: first list entry of tile j
-    count = __shfl_sync(kFull, incl, 31);
-    if (!(over || count < p.K || count > kCap)) {
-      const uint32_t top_bin = f32_key(__fadd_rn(cum, __fsub_rn(top, lse))) >> 16;
-      for (int e0 = 0; e0 < count; e0 += 8 * kFinalThreads) {
-        unsigned long long v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int e = e0 + k * kFinalThreads + tid;
-          // the tile holding entry e: the last j with start_j <= e
-          int j = 0;
-#pragma unroll
-          for (int stp = 16; stp > 0; stp >>= 1) {
-            const int s_j = __shfl_sync(kFull, st, j + stp);
-            if (j + stp < nt && s_j <= e) j += stp;
-          }
-          const int sj = __shfl_sync(kFull, st, j);
-          v[k] = (e < count) ? __ldcg(seg + static_cast<int64_t>(j) * p.seg_cap + (e - sj)) : 0ull;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int e = e0 + k * kFinalThreads + tid;
-          if (e < count) {
-            cand[e] = v[k];
-            const uint32_t sk = score_key(v[k], cum, lse);
-            kmax = max(kmax, sk);
-            const uint32_t bin = sk >> 16;
-            const uint32_t d = top_bin - bin;
-            if (d < static_cast<uint32_t>(kLocalBins)) atomicAdd(&sh.lbins[d], 1u);
-            else red_add(p.fine + bin, 1u);
-          }
-        }
-      }
-    }
-  } else {
-    float M = -INFINITY;
-    top = -INFINITY;
-    over = false;
-    for (int j = tid; j < nt; j += kFinalThreads) {
-      const float4 q = __ldcg(P + j);
-      if (q.y > 0.f) M = fmaxf(M, q.x);
-      top = fmaxf(top, q.z);
-      over |= __float_as_int(q.w) > p.seg_cap;
-    }
-    M = block_max(M, sh);
-    top = block_max(top, sh);
-    over = __syncthreads_or(over);
-    float L = 0.f;
-    for (int j = tid; j < nt; j += kFinalThreads) {
-      const float4 q = __ldcg(P + j);
-      if (q.y > 0.f) L += q.y * ex2((q.x - M) * kLog2e);
-    }
-    L = block_sum(L, sh);
-    lse = M + logf(L);
-    // segment starts (exclusive prefix of the tiles' counts)
-    int carry = 0;
-    for (int j0 = 0; j0 < nt; j0 += kFinalThreads) {
-      const int j = j0 + tid;
-      const int cj = (j < nt) ? __float_as_int(__ldcg(&P[j].w)) : 0;
-      int tot;
-      const int ex = block_scan_excl(cj, &tot, sh);
-      if (j < nt) start[j] = carry + ex;
-      carry += tot;
-    }
-    if (tid == 0) start[nt] = carry;
-    __syncthreads();
-    count = carry;
-    if (!(over || count < p.K || count > kCap)) {
-      const uint32_t top_bin = f32_key(__fadd_rn(cum, __fsub_rn(top, lse))) >> 16;
-      for (int e = tid; e < count; e += kFinalThreads) {
-        int lo = 0, hi = nt - 1;  // the tile whose segment holds entry e
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if (start[mid] <= e) lo = mid;
-          else hi = mid - 1;
-        }
-        const unsigned long long entry = __ldcg(seg + static_cast<int64_t>(lo) * p.seg_cap + (e - start[lo]));
-        cand[e] = entry;
-        const uint32_t sk = score_key(entry, cum, lse);
-        kmax = max(kmax, sk);
-        const uint32_t bin = sk >> 16;
-        const uint32_t d = top_bin - bin;
-        if (d < static_cast<uint32_t>(kLocalBins)) atomicAdd(&sh.lbins[d], 1u);
-        else red_add(p.fine + bin, 1u);
-      }
-    }
+  float M = -INFINITY;
+  for (int j = lane; j < nt; j += 32) {
+    const float2 q = __ldcg(P + j);
+    if (q.y > 0.f) M = fmaxf(M, q.x);
   }
-  if (tid == 0) {
+  M = warp_max(M);
+  float L = 0.f;
+  for (int j = lane; j < nt; j += 32) {
+    const float2 q = __ldcg(P + j);
+    if (q.y > 0.f) L += q.y * ex2((q.x - M) * kLog2e);
+  }
+  L = warp_sum(L);
+  const float lse = (L > 0.f) ? M + logf(L) : -INFINITY;
+  if (lane == 0 && (!sub_level || warp == 0)) {
     p.lse[b] = lse;
     if (p.out_lse) p.out_lse[b] = lse;
   }
-  // the row maximum is a candidate, so its score is the beam's largest
-  uint32_t top_bin = f32_key(__fadd_rn(cum, __fsub_rn(top, lse))) >> 16;
-  if (over || count < p.K || count > kCap) {
-    // the threshold missed: the exact top K from the whole row
-    exact_beam(p, sh, b);
-    count = p.K;
-    for (int i = tid; i < count; i += kFinalThreads) kmax = max(kmax, score_key(__ldcg(cand + i), cum, lse));
-    // the window starts at the largest key of the exact list itself
-    const uint32_t kb = block_max_u32(kmax, sh);
-    top_bin = kb >> 16;
-    for (int i = tid; i < count; i += kFinalThreads) {
-      const uint32_t sk = score_key(__ldcg(cand + i), cum, lse);
-      kmax = max(kmax, sk);
-      const uint32_t bin = sk >> 16;
-      const uint32_t d = top_bin - bin;
-      if (d < static_cast<uint32_t>(kLocalBins)) atomicAdd(&sh.lbins[d], 1u);
-      else red_add(p.fine + bin, 1u);
+  uint32_t kmax = 0u;
+  if (!sub_level) {
+    for (int j0 = 0; j0 < nt; j0 += 32) {
+      const int j = j0 + lane;
+      const bool valid = j < nt;
+      const uint32_t key = valid ? score_key_x(__ldcg(&P[j].x), cum, lse) : 0u;
+      if (valid) p.gkeys[static_cast<int64_t>(b) * nt + j] = key;
+      hist_add(p.hist, key, valid);
+      kmax = max(kmax, key);
     }
-  } else if (tid == 0) {
-    p.cand_count[b] = count;
+  } else {
+    const int n = nt * kSubPerTile;
+    const uint16_t* sm = p.submax + static_cast<int64_t>(b) * n;
+    uint32_t* gk = p.gkeys + static_cast<int64_t>(b) * n;
+    for (int i0 = warp * 32; i0 < n; i0 += kRowThreads) {
+      const int i = i0 + lane;
+      const bool valid = i < n;
+      const uint32_t key = valid ? score_key_x(bf16_bits_to_f32(__ldcg(sm + i)), cum, lse) : 0u;
+      if (valid) gk[i] = key;
+      hist_add(p.hist, key, valid);
+      kmax = max(kmax, key);
+    }
   }
-  __syncthreads();
-  for (int d = tid; d < kLocalBins; d += kFinalThreads) {
-    const unsigned v = sh.lbins[d];
-    if (v) red_add(p.fine + (top_bin - d), v);
-  }
-  // the global walk starts at the largest key actually histogrammed (with
-  // finite logits that of the row maximum; it also bounds NaN-derived keys)
   kmax = warp_max_u32(kmax);
   if (lane == 0) atomicMax(p.misc + kMiscMaxKey, kmax);
 }
 
 // ---------------------------------------------------------------------------
-// 4. final
+// 3. select
 // ---------------------------------------------------------------------------
-constexpr int kRankBins = 1024;  // score bins the final ranking spans without a full sort
+constexpr int kBins = 4096;                      // final ranking bins
+constexpr int kUnitWords = 16384;                // ballot words: groups up to 524,288
+constexpr int kBinsPerThread = kBins / kSelThreads;
+static_assert(kBins % kSelThreads == 0, "whole bins per thread");
+static_assert(kUnitCap >= kCandCap, "the final ranking's order fits the group list");
 
-// Dynamic shared memory of the final kernel: this head, then elite_cap
-// entries (as ulonglong2, or as separate hi / lo arrays for the ranking).
-struct FinalHead {
+// Dynamic shared memory of the select kernel.
+struct SelSmem {
+  float lse[kMaxRows];
+  float cum[kMaxRows];
+  int units[kUnitCap];        // groups scoring >= L (tiles, or sub-chunks t * 128 + s); the final ranking's lists
+  unsigned bins[kBins];
+  int fill[kBins];
+  int rtok[2048], rpar[2048];  // the K results, written out together
+  float rsc[2048];
+  union {
+    struct {
+      unsigned long long hi[kCandCap];
+      uint32_t lo[kCandCap];
+    } c;                        // the last CTA's candidates, while they are ranked
+    ulonglong2 ent[kCandCap];   // the exact path's result, while it is sorted
+    unsigned whist[kSelWarps][256];  // the exact path's radix histograms
+    uint32_t words[kUnitWords];      // ballot words of the groups scoring >= L
+  } u;
   Scratch sc;
-  int pre[kRankBins];   // entries of the list in bins above bin S - d
-  int fill[kRankBins];  // entries placed so far in bin S - d
 };
 
-// Result r of the global order; error = true writes -1 ids and NaN scores.
-__device__ __forceinline__ void write_result(const Params& p, int r, const ulonglong2& g, bool error = false) {
-  const int token = error ? -1 : static_cast<int>(0xFFFFFFFFull - g.y);
-  const int parent = error ? -1 : 0xFFFF - static_cast<int>((g.x >> 16) & 0xFFFFull);
-  const float score = error ? __int_as_float(0x7fc00000) : key_to_f32(static_cast<uint32_t>(g.x >> 32));
-  if (r < p.W) {
-    p.out_token[r] = token;
-    p.out_parent[r] = parent;
-    p.out_score[r] = score;
-  }
-  if (p.out_cand_token) p.out_cand_token[r] = token;
-  if (p.out_cand_parent) p.out_cand_parent[r] = parent;
-  if (p.out_cand_score) p.out_cand_score[r] = score;
+// Result r of the global order into shared memory; error = true: -1 ids and NaN scores.
+__device__ __forceinline__ void stage_result(SelSmem& sm, int r, const ulonglong2& g, bool error = false) {
+  sm.rtok[r] = error ? -1 : static_cast<int>(0xFFFFFFFFull - g.y);
+  sm.rpar[r] = error ? -1 : 0xFFFF - static_cast<int>((g.x >> 16) & 0xFFFFull);
+  sm.rsc[r] = error ? __int_as_float(0x7fc00000) : key_to_f32(static_cast<uint32_t>(g.x >> 32));
 }
 
-__global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  FinalHead& fs = *reinterpret_cast<FinalHead*>(smem_raw);
-  Scratch& sh = fs.sc;
-  ulonglong2* ent = reinterpret_cast<ulonglong2*>(smem_raw + sizeof(FinalHead));
-  const int cap = p.elite_cap;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int K = p.K;
-  const int b = blockIdx.x;
-  grid_dep_wait();
+__device__ __forceinline__ void write_results(const Params& p, const SelSmem& sm) {
+  __syncthreads();
+  for (int r = threadIdx.x; r < p.K; r += kSelThreads) {
+    if (r < p.W) {
+      p.out_token[r] = sm.rtok[r];
+      p.out_parent[r] = sm.rpar[r];
+      p.out_score[r] = sm.rsc[r];
+    }
+    if (p.out_cand_token) p.out_cand_token[r] = sm.rtok[r];
+    if (p.out_cand_parent) p.out_cand_parent[r] = sm.rpar[r];
+    if (p.out_cand_score) p.out_cand_score[r] = sm.rsc[r];
+  }
+}
 
-  // everything this CTA reads, requested at once: its beam's values, the
-  // first candidates (the list buffer is always that long), the top key
-  constexpr int kBatch = 8;
-  const unsigned long long* cand = p.cand + static_cast<int64_t>(b) * kCap;
-  unsigned long long e[kBatch];
+__device__ __forceinline__ void write_errors(const Params& p, SelSmem& sm) {
+  for (int r = threadIdx.x; r < p.K; r += kSelThreads) stage_result(sm, r, make_ulonglong2(0ull, 0ull), true);
+  write_results(p, sm);
+}
+
+// Eight logits of row b at columns col .. col + 7 (as four bf16x2 words);
+// columns at or past V read as -inf.
+__device__ __forceinline__ uint4 load_run(const Params& p, int b, int col) {
+  const uint16_t* row = p.logits + static_cast<int64_t>(b) * p.V;
+  if (p.vec_ok && col + 8 <= p.V) return __ldcs(reinterpret_cast<const uint4*>(row + col));
+  uint32_t w[4];
 #pragma unroll
-  for (int k = 0; k < kBatch; ++k) e[k] = __ldcg(cand + k * kFinalThreads + tid);
-  const int count = min(__ldcg(p.cand_count + b), kCap);
-  const float lse = __ldcg(p.lse + b), cum = __ldg(p.cum + b);
-  const int S = static_cast<int>(__ldcg(p.misc + kMiscMaxKey) >> 16);
+  for (int h = 0; h < 4; ++h) {
+    const uint32_t lo = (col + 2 * h < p.V) ? row[col + 2 * h] : 0xFF80u;
+    const uint32_t hi = (col + 2 * h + 1 < p.V) ? row[col + 2 * h + 1] : 0xFF80u;
+    w[h] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
 
-  // B*: walking the histogram down from the largest score, the bin where the
-  // running count first reaches K.  pre[] keeps the running counts of the
-  // bins walked (for the ranking by the last CTA).
-  {
-    int top = S, carry = 0;
-    if (tid == 0) sh.bstar = -1;
-    while (true) {
+__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
+  Scratch& sh = sm.sc;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int K = p.K, nt = p.n_tpr;
+  // inputs that do not come from the previous kernels: before the wait
+  for (int b = tid; b < p.W_in; b += kSelThreads) sm.cum[b] = __ldg(p.cum + b);
+  for (int i = tid; i < kBins; i += kSelThreads) {
+    sm.bins[i] = 0u;
+    sm.fill[i] = 0;
+  }
+  grid_dep_wait();
+  for (int b = tid; b < p.W_in; b += kSelThreads) sm.lse[b] = __ldcg(p.lse + b);
+  const uint32_t maxkey = __ldcg(p.misc + kMiscMaxKey);
+
+  // the groups: tiles when there are at least K of them, else sub-chunks
+  const bool tile_level = p.n_tiles >= K;
+  const int n_groups = tile_level ? p.n_tiles : p.n_tiles * kSubPerTile;
+
+  // L: the lower edge of the histogram bin that holds the K-th largest group
+  // key (bins walked down from the largest key's) -- at most that key, so at
+  // least K groups score >= L.  At most K groups: all of them.
+  uint32_t Lk = 0u;
+  if (n_groups > K) {
+    int carry = 0;
+    if (tid == 0) sh.dstar = -1;
+    for (int top = static_cast<int>(maxkey >> 16); top >= 0; top -= kSelThreads) {
       const int bin = top - tid;
-      const int c = (bin >= 0) ? static_cast<int>(__ldcg(p.fine + bin)) : 0;
+      const int c = (bin >= 0) ? static_cast<int>(__ldcg(p.hist + bin)) : 0;
       int total;
-      const int excl = block_scan_excl(c, &total, sh);
-      if (S - bin < kRankBins) fs.pre[S - bin] = carry + excl;
-      if (carry + excl < K && carry + excl + c >= K) {
-        sh.bstar = bin;
-        sh.bstar_above = carry + excl;
-        sh.bstar_count = c;
-      }
+      const int ex = block_scan_excl(c, &total, sh);
+      if (carry + ex < K && carry + ex + c >= K) sh.dstar = bin;
       carry += total;
-      if (carry >= K || top - kFinalThreads < 0) break;
-      top -= kFinalThreads;
+      if (carry >= K) break;  // uniform
+    }
+    __syncthreads();
+    if (sh.dstar >= 0) Lk = static_cast<uint32_t>(sh.dstar) << 16;
+  }
+
+  // the groups scoring >= L, in group order (every CTA builds the same list
+  // and takes its share of it): each warp reads a contiguous range once,
+  // keeping one ballot word per 32 groups in shared memory
+  int n_found;
+  {
+    uint32_t* words = sm.u.words;
+    const int n_words = min((n_groups + 31) >> 5, kUnitWords);  // more groups: the exact path
+    const int per = (n_words + kSelWarps - 1) / kSelWarps;  // words per warp
+    const int w_lo = min(n_words, warp * per), w_hi = min(n_words, w_lo + per);
+    int cnt = 0;
+    for (int w0 = w_lo; w0 < w_hi; w0 += 8) {
+      uint32_t k8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int g = (w0 + i) * 32 + lane;
+        k8[i] = (w0 + i < w_hi && g < n_groups) ? __ldcg(p.gkeys + g) : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int g = (w0 + i) * 32 + lane;
+        const unsigned bal = __ballot_sync(kFull, w0 + i < w_hi && g < n_groups && k8[i] >= Lk);
+        if (w0 + i < w_hi && lane == 0) words[w0 + i] = bal;
+        cnt += __popc(bal);
+      }
+    }
+    if (lane == 0) sh.wint[warp] = cnt;
+    __syncthreads();
+    int pos = 0;
+    n_found = 0;
+    for (int i = 0; i < kSelWarps; ++i) {
+      if (i < warp) pos += sh.wint[i];
+      n_found += sh.wint[i];
+    }
+    for (int wd = w_lo; wd < w_hi; ++wd) {
+      const unsigned bal = words[wd];
+      const int at = pos + __popc(bal & ((1u << lane) - 1u));
+      if (((bal >> lane) & 1u) && at < kUnitCap) sm.units[at] = wd * 32 + lane;
+      pos += __popc(bal);
     }
     __syncthreads();
   }
-  const int bstar = sh.bstar;
-  if (bstar < 0 && tid == 0) atomicOr(p.misc + kMiscStatus, 2u);
+  const int n_units = min(n_found, kUnitCap);
+  const bool unit_over = n_found > kUnitCap || ((n_groups + 31) >> 5) > kUnitWords;
 
-  // this beam's candidates in bins >= B* to the final list
-  if (bstar >= 0) {
-    for (int i0 = 0; i0 < count; i0 += kBatch * kFinalThreads) {
-      if (i0 > 0) {
+  // Read back this CTA's share of the sub-chunks scoring >= L and append their
+  // logits scoring >= L.  A warp handles up to four sub-chunks at once, eight
+  // lanes each, one 16-byte run of eight logits per lane.
+  if (!unit_over) {
+    const int wg = blockIdx.x * kSelWarps + warp, n_wg = gridDim.x * kSelWarps;
+    for (int u = wg; u < n_units; u += n_wg) {
+      const int g = sm.units[u];
+      const int t = tile_level ? g : g / kSubPerTile;
+      const int b = t / nt, c = t - b * nt;
+      const float cum = sm.cum[b], lse = sm.lse[b];
+      // the tile's sub-chunks scoring >= L, as four lane masks (q = 0..3)
+      unsigned mq[kQuarters];
+      if (tile_level) {
+        const uint16_t* smx = p.submax + static_cast<int64_t>(t) * kSubPerTile;
 #pragma unroll
-        for (int k = 0; k < kBatch; ++k) {
-          const int i = i0 + k * kFinalThreads + tid;
-          e[k] = (i < count) ? __ldcg(cand + i) : 0ull;
-        }
+        for (int q = 0; q < kQuarters; ++q)
+          mq[q] = __ballot_sync(kFull, score_key_x(bf16_bits_to_f32(__ldcg(smx + q * 32 + lane)), cum, lse) >= Lk);
+      } else {
+        const int s = g - t * kSubPerTile;
+#pragma unroll
+        for (int q = 0; q < kQuarters; ++q) mq[q] = (q == s / 32) ? (1u << (s % 32)) : 0u;
       }
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k) {
-        if (i0 + k * kFinalThreads >= count) break;  // uniform across the CTA
-        const int i = i0 + k * kFinalThreads + tid;
-        bool take = false;
-        ulonglong2 g = make_ulonglong2(0ull, 0ull);
-        if (i < count) {
-          const uint32_t sk = score_key(e[k], cum, lse);
-          if (static_cast<int>(sk >> 16) >= bstar) {
-            take = true;
-            g = global_entry(sk, static_cast<uint32_t>(b), e[k]);
-          }
+      const int n0 = __popc(mq[0]), n1 = __popc(mq[1]), n2 = __popc(mq[2]);
+      const int n_sub = n0 + n1 + n2 + __popc(mq[3]);
+      for (int base = 0; base < n_sub; base += 4) {
+        const int j = base + (lane >> 3), r = lane & 7;  // sub-chunk j of the list, run r
+        int cnt = 0;
+        uint4 x = make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+        int col = 0;
+        if (j < n_sub) {
+          int q = 0, k = j;
+          unsigned m = mq[0];
+          if (k >= n0) { k -= n0; q = 1; m = mq[1];
+            if (k >= n1) { k -= n1; q = 2; m = mq[2];
+              if (k >= n2) { k -= n2; q = 3; m = mq[3]; } } }
+          for (int i = 0; i < k; ++i) m &= m - 1u;  // drop the k lowest set bits
+          const int l = __ffs(m) - 1;
+          col = c * kTile + sub_run_offset(q, l, r);
+          x = load_run(p, b, col);
         }
-        const unsigned bal = __ballot_sync(kFull, take);
-        if (bal) {
-          unsigned base = 0;
-          if (lane == 0) base = atomicAdd(p.misc + kMiscElite, static_cast<unsigned>(__popc(bal)));
-          base = __shfl_sync(kFull, base, 0);
-          const unsigned pos = base + __popc(bal & ((1u << lane) - 1u));
-          if (take && pos < static_cast<unsigned>(cap)) p.elite[pos] = g;
+        const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+        uint32_t keys[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          keys[h] = score_key_x(bf16_bits_to_f32((h & 1) ? (wd[h >> 1] >> 16) : (wd[h >> 1] & 0xFFFFu)), cum, lse);
+          cnt += (j < n_sub && keys[h] >= Lk);
+        }
+        const int incl = warp_inclusive_scan(cnt, lane);
+        const int total = __shfl_sync(kFull, incl, 31);
+        if (total == 0) continue;
+        unsigned pos0 = 0;
+        if (lane == 0) pos0 = atomicAdd(p.misc + kMiscCand, static_cast<unsigned>(total));
+        int pos = static_cast<int>(__shfl_sync(kFull, pos0, 0)) + incl - cnt;
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          if (j < n_sub && keys[h] >= Lk) {
+            if (pos < kCandCap) {
+              const uint32_t bits = (h & 1) ? (wd[h >> 1] >> 16) : (wd[h >> 1] & 0xFFFFu);
+              p.cand[pos] = global_entry(keys[h], static_cast<uint32_t>(b),
+                                         cand_entry(bits, static_cast<uint32_t>(col + h)));
+            }
+            ++pos;
+          }
         }
       }
     }
@@ -1066,114 +918,139 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
 
   // the last CTA to finish ranks the list
   __syncthreads();
-  if (tid == 0) sh.flag = (atom_add_acq_rel(p.misc + kMiscTicket, 1u) == gridDim.x - 1);
+  if (tid == 0) {
+    __threadfence();
+    sh.flag = (atom_add_acq_rel(p.misc + kMiscTicket, 1u) == gridDim.x - 1);
+  }
   __syncthreads();
   if (!sh.flag) return;
 
-  const unsigned status = __ldcg(p.misc + kMiscStatus);
-  const int n_e = static_cast<int>(__ldcg(p.misc + kMiscElite));
-  // the list holds exactly the histogram's entries in bins >= B*
-  if (status != 0u || bstar < 0 || n_e < K || n_e != sh.bstar_above + sh.bstar_count) {
-    for (int r = tid; r < K; r += kFinalThreads) write_result(p, r, make_ulonglong2(0ull, 0ull), true);
+  if (__ldcg(p.misc + kMiscStatus) != 0u) {
+    write_errors(p, sm);
     return;
   }
-
-  if (n_e <= cap && S - bstar < kRankBins) {
-    // Rank by bin: an entry's place is the count of the bins above its own
-    // plus its rank among the (few) entries of its bin.  Entries are first
-    // grouped by bin, then each compares itself with its group.
-    unsigned long long* ehi = reinterpret_cast<unsigned long long*>(ent);
-    uint32_t* elo = reinterpret_cast<uint32_t*>(ehi + cap);
-    for (int d = tid; d <= S - bstar; d += kFinalThreads) fs.fill[d] = 0;
-    if (tid == 0) sh.counter = 0;  // entries outside [B*, S]: none unless the histogram is inconsistent
-    __syncthreads();
-    for (int i = tid; i < n_e; i += kFinalThreads) {
-      const unsigned long long hi = __ldcg(&p.elite[i].x);
-      const uint32_t lo = static_cast<uint32_t>(__ldcg(&p.elite[i].y));
-      const int d = S - static_cast<int>(hi >> 48);
-      if (d < 0 || d > S - bstar) {
-        atomicAdd(&sh.counter, 1);
-        continue;
-      }
-      const int idx = fs.pre[d] + atomicAdd(&fs.fill[d], 1);
-      if (idx < cap) {
-        ehi[idx] = hi;
-        elo[idx] = lo;
-      }
-    }
-    __syncthreads();
-    if (sh.counter != 0) {
-      for (int r = tid; r < K; r += kFinalThreads) write_result(p, r, make_ulonglong2(0ull, 0ull), true);
+  const int n_cand = static_cast<int>(__ldcg(p.misc + kMiscCand));
+  if (!unit_over && n_cand <= kCandCap) {
+    if (n_cand < K) {  // cannot happen: every group scoring >= L holds one candidate
+      write_errors(p, sm);
       return;
     }
-    for (int i = tid; i < n_e; i += kFinalThreads) {
-      const unsigned long long hi = ehi[i];
-      const uint32_t lo = elo[i];
-      const int d = S - static_cast<int>(hi >> 48);
-      const int g0 = fs.pre[d], gn = fs.fill[d];
-      int rank = g0;
-      const int g1 = min(g0 + gn, n_e);
-#pragma unroll 4
-      for (int j = g0; j < g1; ++j) {
-        const unsigned long long hj = ehi[j];
-        rank += (hj > hi) | ((hj == hi) & (elo[j] > lo));
-      }
-      if (rank < K) write_result(p, rank, make_ulonglong2(hi, lo));
+    // Rank by bin: an entry's place is the count of the entries in the bins
+    // above its own (bins of the score key counted down from the largest,
+    // all scores >= L spread over kBins bins) plus its rank among the
+    // entries of its own bin.
+    const unsigned long long range = static_cast<unsigned long long>(maxkey - min(Lk, maxkey));
+    const int s2 = max(0, 64 - __clzll(range + 1ull) - 12);  // (range >> s2) < kBins
+    auto bin_of = [&](unsigned long long hi) -> uint32_t {
+      const uint32_t skey = static_cast<uint32_t>(hi >> 32);
+      return min(static_cast<uint32_t>(static_cast<unsigned long long>(maxkey - min(skey, maxkey)) >> s2),
+                 static_cast<uint32_t>(kBins - 1));
+    };
+    for (int i = tid; i < n_cand; i += kSelThreads) {
+      const unsigned long long hi = __ldcg(&p.cand[i].x);
+      sm.u.c.hi[i] = hi;
+      sm.u.c.lo[i] = static_cast<uint32_t>(__ldcg(&p.cand[i].y));
+      atomicAdd(&sm.bins[bin_of(hi)], 1u);
     }
+    __syncthreads();
+    // bins -> first position of each bin (fill[] keeps the counts)
+    int* order = sm.units;  // entries grouped by bin
+    {
+      const int d0 = tid * kBinsPerThread;
+      int cnt = 0;
+#pragma unroll
+      for (int i = 0; i < kBinsPerThread; ++i) cnt += static_cast<int>(sm.bins[d0 + i]);
+      int total;
+      int c = block_scan_excl(cnt, &total, sh);
+#pragma unroll
+      for (int i = 0; i < kBinsPerThread; ++i) {
+        const int v = static_cast<int>(sm.bins[d0 + i]);
+        sm.fill[d0 + i] = v;
+        sm.bins[d0 + i] = static_cast<unsigned>(c);
+        c += v;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < n_cand; i += kSelThreads) {
+      const uint32_t d = bin_of(sm.u.c.hi[i]);
+      order[static_cast<int>(atomicAdd(&sm.bins[d], 1u))] = i;  // bins[d] ends one past the bin
+    }
+    __syncthreads();
+    // Each entry's rank: the entries of the bins above, plus those of its own
+    // bin that come before it.
+    for (int i = tid; i < n_cand; i += kSelThreads) {
+      const unsigned long long hi = sm.u.c.hi[i];
+      const uint32_t lo = sm.u.c.lo[i];
+      const uint32_t d = bin_of(hi);
+      const int g1 = static_cast<int>(sm.bins[d]), g0 = g1 - sm.fill[d];
+      int rank = g0;
+      for (int j = g0; j < g1; ++j) {
+        const int o = order[j];
+        const unsigned long long hj = sm.u.c.hi[o];
+        rank += (hj > hi) | ((hj == hi) & (sm.u.c.lo[o] > lo));
+      }
+      if (rank < K) stage_result(sm, rank, make_ulonglong2(hi, lo));
+    }
+    write_results(p, sm);
     return;
   }
 
-  int n_sort;
-  if (n_e <= cap) {
-    n_sort = n_e;
-    for (int i = tid; i < n_e; i += kFinalThreads) {
-      ulonglong2 g;
-      g.x = __ldcg(&p.elite[i].x);
-      g.y = __ldcg(&p.elite[i].y);
-      ent[i] = g;
-    }
-  } else {
-    // Huge score ties: exact selection over every candidate in bins >= B*.
-    auto for_each_entry = [&](auto f) {
-      for (int bb = 0; bb < p.W_in; ++bb) {
-        const int cnt = min(__ldcg(p.cand_count + bb), kCap);
-        const float lse_b = __ldcg(p.lse + bb), cum_b = __ldg(p.cum + bb);
-        const unsigned long long* cd = p.cand + static_cast<int64_t>(bb) * kCap;
-        for (int i = tid; i < cnt; i += kFinalThreads) {
-          const unsigned long long en = __ldcg(cd + i);
-          const uint32_t sk = score_key(en, cum_b, lse_b);
-          if (static_cast<int>(sk >> 16) >= bstar) f(global_entry(sk, static_cast<uint32_t>(bb), en));
+  // Huge score ties: every logit scoring >= L, ranked exactly.  The groups
+  // scoring >= L are found again (the list may have overflowed), and all of
+  // their logits are visited.
+  const int group_size = tile_level ? kTile : 64;
+  const int n_scan = unit_over ? n_groups : n_units;
+  auto for_each_entry = [&](auto f) {
+    for (int u = 0; u < n_scan; ++u) {
+      const int g = unit_over ? u : sm.units[u];
+      if (unit_over && __ldcg(p.gkeys + g) < Lk) continue;  // uniform: every thread reads the same key
+      const int t = tile_level ? g : g / kSubPerTile;
+      const int b = t / nt, c = t - b * nt;
+      const float cum = sm.cum[b], lse = sm.lse[b];
+      const uint16_t* row = p.logits + static_cast<int64_t>(b) * p.V;
+      for (int e = tid; e < group_size; e += kSelThreads) {
+        int off;
+        if (tile_level) {
+          off = e;
+        } else {
+          const int s = g - t * kSubPerTile;
+          off = sub_run_offset(s / 32, s % 32, e >> 3) + (e & 7);
         }
+        const int col = c * kTile + off;
+        if (col >= p.V) continue;
+        const uint32_t bits = __ldcg(row + col);
+        const uint32_t key = score_key_x(bf16_bits_to_f32(bits), cum, lse);
+        if (key >= Lk) f(global_entry(key, static_cast<uint32_t>(b), cand_entry(bits, static_cast<uint32_t>(col))));
       }
-    };
-    const unsigned long long kth_hi =
-        block_kth([&](auto f) { for_each_entry([&](const ulonglong2& g) { f(g.x); }); }, K, sh);
-    int mine = 0;
-    for_each_entry([&](const ulonglong2& g) { mine += (g.x > kth_hi); });
-    int above;
-    block_scan_excl(mine, &above, sh);
-    const unsigned long long kth_lo = block_kth(
-        [&](auto f) {
-          for_each_entry([&](const ulonglong2& g) {
-            if (g.x == kth_hi) f(g.y);
-          });
-        },
-        K - above, sh);
-    if (tid == 0) sh.counter = 0;
-    __syncthreads();
-    for_each_entry([&](const ulonglong2& g) {
-      if (g.x > kth_hi || (g.x == kth_hi && g.y >= kth_lo)) {
-        const int pos = atomicAdd(&sh.counter, 1);
-        if (pos < cap) ent[pos] = g;
-      }
-    });
-    __syncthreads();
-    n_sort = K;
-  }
-  const int n2 = next_pow2(max(n_sort, 2));
-  for (int i = n_sort + tid; i < n2; i += kFinalThreads) ent[i] = make_ulonglong2(0ull, 0ull);
-  block_sort_desc(ent, n2);
-  for (int r = tid; r < K; r += kFinalThreads) write_result(p, r, ent[r]);
+    }
+  };
+  const unsigned long long kth_hi =
+      block_kth([&](auto f) { for_each_entry([&](const ulonglong2& g) { f(g.x); }); }, K, sh, sm.u.whist);
+  int mine = 0;
+  for_each_entry([&](const ulonglong2& g) { mine += (g.x > kth_hi); });
+  int above;
+  block_scan_excl(mine, &above, sh);
+  const unsigned long long kth_lo = block_kth(
+      [&](auto f) {
+        for_each_entry([&](const ulonglong2& g) {
+          if (g.x == kth_hi) f(g.y);
+        });
+      },
+      K - above, sh, sm.u.whist);
+  if (tid == 0) sh.counter = 0;
+  __syncthreads();
+  for_each_entry([&](const ulonglong2& g) {
+    if (g.x > kth_hi || (g.x == kth_hi && g.y >= kth_lo)) {
+      const int pos = atomicAdd(&sh.counter, 1);
+      if (pos < kCandCap) sm.u.ent[pos] = g;
+    }
+  });
+  __syncthreads();
+  const int n2 = next_pow2(max(K, 2));
+  for (int i = K + tid; i < n2; i += kSelThreads) sm.u.ent[i] = make_ulonglong2(0ull, 0ull);
+  block_sort_desc(sm.u.ent, n2);
+  for (int r = tid; r < K; r += kSelThreads) stage_result(sm, r, sm.u.ent[r]);
+  write_results(p, sm);
 }
 
 }  // namespace sel
@@ -1184,8 +1061,8 @@ __global__ void __launch_bounds__(kFinalThreads, 1) final_kernel(const Params p)
 namespace {
 
 struct SelLayout {
-  int n_tpr, seg_cap, elite_cap;
-  size_t off_tau, off_ref, off_lse, off_count, off_seg, off_partial, off_cand, off_fine, off_misc, off_elite, total;
+  int n_tpr;
+  size_t off_partial, off_submax, off_lse, off_gkeys, off_hist, off_cand, off_misc, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -1193,25 +1070,17 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 bool sel_layout(int W_in, int V, int W, SelLayout* L) {
   if (W_in <= 0 || V <= 0 || W <= 0) return false;
   const int64_t K = 2 * static_cast<int64_t>(W);
-  if (K > 2048 || K > V || W_in > 1024 || V >= (1 << 24)) return false;
+  if (K > 2048 || K > V || W_in > sel::kMaxRows || V >= (1 << 24)) return false;
   L->n_tpr = (V + sel::kTile - 1) / sel::kTile;
-  // a row of one tile keeps every logit (tau = -inf)
-  L->seg_cap = (L->n_tpr == 1) ? ((V + 7) & ~7) : sel::kSegCap;
+  const size_t n_tiles = size_t(W_in) * L->n_tpr;
   size_t o = 0;
-  L->off_tau = o;     o = align256(o + sizeof(float) * size_t(W_in));
-  L->off_ref = o;     o = align256(o + sizeof(float) * size_t(W_in));
+  L->off_partial = o; o = align256(o + sizeof(float2) * n_tiles);
+  L->off_submax = o;  o = align256(o + sizeof(uint16_t) * n_tiles * sel::kSubPerTile);
   L->off_lse = o;     o = align256(o + sizeof(float) * size_t(W_in));
-  L->off_count = o;   o = align256(o + sizeof(int) * size_t(W_in));
-  L->off_seg = o;     o = align256(o + sizeof(unsigned long long) * size_t(W_in) * L->n_tpr * L->seg_cap);
-  L->off_partial = o; o = align256(o + sizeof(float4) * size_t(W_in) * L->n_tpr);
-  L->off_cand = o;    o = align256(o + sizeof(unsigned long long) * size_t(W_in) * sel::kCap);
-  L->off_fine = o;    o = align256(o + sizeof(unsigned) * size_t(sel::kFineBins));
-  L->off_misc = o;    o = align256(o + sizeof(unsigned) * 4);
-  // the final list: 2K entries and room for a few ties, a power of two
-  int cap = 512;
-  while (cap < 2 * K && cap < sel::kEliteMax) cap <<= 1;
-  L->elite_cap = cap;
-  L->off_elite = o;   o = align256(o + sizeof(ulonglong2) * size_t(cap));
+  L->off_gkeys = o;   o = align256(o + sizeof(uint32_t) * n_tiles * sel::kSubPerTile);
+  L->off_hist = o;    o = align256(o + sizeof(unsigned) * size_t(sel::kHistBins));
+  L->off_cand = o;    o = align256(o + sizeof(ulonglong2) * size_t(sel::kCandCap));
+  L->off_misc = o;    o = align256(o + sizeof(unsigned) * sel::kMiscWords);
   L->total = o;
   return true;
 }
@@ -1228,24 +1097,6 @@ int sm_count() {
     cached[dev] = n;
   }
   return cached[dev];
-}
-
-// Launches a kernel that may start while the previous kernel on the stream is
-// still running; it waits for that kernel's results with griddepcontrol.wait.
-template <class Kernel>
-cudaError_t launch_dependent(Kernel kernel, int grid, int block, size_t smem, cudaStream_t stream,
-                             const sel::Params& p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(block);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 }  // namespace
@@ -1277,19 +1128,14 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   p.W = W;
   p.n_tpr = L.n_tpr;
   p.n_tiles = W_in * L.n_tpr;
-  p.seg_cap = L.seg_cap;
-  p.elite_cap = L.elite_cap;
   p.vec_ok = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
-  p.tau = reinterpret_cast<float*>(ws + L.off_tau);
-  p.ref = reinterpret_cast<float*>(ws + L.off_ref);
+  p.partial = reinterpret_cast<float2*>(ws + L.off_partial);
+  p.submax = reinterpret_cast<uint16_t*>(ws + L.off_submax);
   p.lse = reinterpret_cast<float*>(ws + L.off_lse);
-  p.cand_count = reinterpret_cast<int*>(ws + L.off_count);
-  p.cand = reinterpret_cast<unsigned long long*>(ws + L.off_cand);
-  p.seg = reinterpret_cast<unsigned long long*>(ws + L.off_seg);
-  p.partial = reinterpret_cast<float4*>(ws + L.off_partial);
-  p.fine = reinterpret_cast<unsigned*>(ws + L.off_fine);
+  p.gkeys = reinterpret_cast<uint32_t*>(ws + L.off_gkeys);
+  p.hist = reinterpret_cast<unsigned*>(ws + L.off_hist);
+  p.cand = reinterpret_cast<ulonglong2*>(ws + L.off_cand);
   p.misc = reinterpret_cast<unsigned*>(ws + L.off_misc);
-  p.elite = reinterpret_cast<ulonglong2*>(ws + L.off_elite);
   p.out_token = out_token;
   p.out_parent = out_parent;
   p.out_score = out_score;
@@ -1298,27 +1144,38 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   p.out_cand_score = out_cand_score;
   p.out_lse = out_lse;
 
-  sel::prep_kernel<<<W_in, sel::kPrepThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
+  // The stream kernel is an ordinary launch: it starts after everything
+  // before it on the stream, including a previous call reading this workspace.
   const size_t smem_stream = sizeof(sel::StreamSmem);
-  e = cudaFuncSetAttribute(sel::stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_stream));
+  cudaError_t e = cudaFuncSetAttribute(sel::stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_stream));
   if (e != cudaSuccess) return e;
   const int grid_stream = std::min(sm_count(), p.n_tiles);
-  e = launch_dependent(sel::stream_kernel, grid_stream, sel::kStreamThreads, smem_stream, stream, p);
+  sel::stream_kernel<<<grid_stream, sel::kStreamThreads, smem_stream, stream>>>(p);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  e = launch_dependent(sel::finish_kernel, W_in, sel::kFinalThreads, 0, stream, p);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(p.n_tiles < p.K ? W_in : (W_in + sel::kRowWarps - 1) / sel::kRowWarps);
+  cfg.blockDim = dim3(sel::kRowThreads);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, sel::rowstat_kernel, p);
   if (e != cudaSuccess) return e;
 
-  const size_t smem_final = sizeof(sel::FinalHead) + sizeof(ulonglong2) * size_t(L.elite_cap);
-  e = cudaFuncSetAttribute(sel::final_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_final));
+  const size_t smem_sel = sizeof(sel::SelSmem);
+  e = cudaFuncSetAttribute(sel::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_sel));
   if (e != cudaSuccess) return e;
-  const int grid_final = W_in;
-  return launch_dependent(sel::final_kernel, grid_final, sel::kFinalThreads, smem_final, stream, p);
+  cfg.gridDim = dim3(sm_count());
+  cfg.blockDim = dim3(sel::kSelThreads);
+  cfg.dynamicSmemBytes = smem_sel;
+  return cudaLaunchKernelEx(&cfg, sel::select_kernel, p);
 }
 
 }  // namespace slm

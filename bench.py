@@ -338,7 +338,7 @@ def measure_decode_loop(dev, bw, seed, stop_id, stream, peaks, flush, reps=20, w
     from attention_packed_varlen_gb300 import _binding as slm
     slm.slm_check_status(loop.status)
     n = bw.steps
-    launches = 4 + 1 + n * (1 + 4 + 1) + ((n + 1) if stop_id is not None else 0)
+    launches = 3 + 1 + n * (1 + 3 + 1) + ((n + 1) if stop_id is not None else 0)
     nbytes = loop_bytes(bw)
     return {"stop_id": stop_id, "decode_steps": n, "graph_us_per_loop": graph_s * 1e6,
             "graph_us_per_decode_step": graph_s * 1e6 / n, "eager_us_per_loop": eager_s * 1e6,
@@ -603,8 +603,8 @@ def run_gpu(args):
         tfl, cores, desc = oracle_prefill_sample(budget_s=args.ref_budget)
         cpu = {"value": tfl, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "cpu": cpu_model()}
 
-    # prefill: schedule + attention; decode step: attention + 4 selection kernels
-    launches_per_step = n_pre * 2 + sum(n_dec) * 5
+    # prefill: schedule + attention; decode step: attention + 3 selection kernels
+    launches_per_step = n_pre * 2 + sum(n_dec) * 4
     peak_sust = peaks["bf16_tflops_sustained"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
