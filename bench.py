@@ -162,7 +162,7 @@ class ClockSampler:
 # DRAM bytes (read + write) per prefill launch on this workload, from an ncu
 # capture of `bench.py --ncu-case prefill` (one layer of the same batch), keyed
 # by the kernel source it was taken on; any other source reports null.
-PREFILL_TRAFFIC = {"2f8683730f323e49": 1.166724e9 + 0.502974e9}
+PREFILL_TRAFFIC = {"2f8683730f323e49": 1.166724e9 + 0.502974e9, "0723e93353cd1195": 1.238973e9 + 0.511833e9}
 
 
 def prefill_traffic():
