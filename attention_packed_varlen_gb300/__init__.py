@@ -17,4 +17,5 @@ from ._binding import (  # noqa: F401
     slm_packed_prefill_attn,
     slm_prefill_workspace_size,
     slm_shared_prefix_decode_attn,
+    slm_shared_prefix_decode_workspace_size,
 )

@@ -25,7 +25,7 @@ STATUS_NAMES = {0: "SLM_OK", 1: "SLM_ERR_INVALID_ARG", 2: "SLM_ERR_UNSUPPORTED",
 EXPORTS = ("slm_last_error", "slm_abi_version", "slm_packed_prefill_attn", "slm_prefill_workspace_size",
            "slm_shared_prefix_decode_attn", "slm_beam_select", "slm_beam_select_workspace_size",
            "slm_check_status", "slm_packed_prefill_attn_noalloc", "slm_swiglu_quant_e4m3", "slm_label_scores",
-           "slm_beam_split_finished", "slm_beam_reorder_history")
+           "slm_beam_split_finished", "slm_beam_reorder_history", "slm_shared_prefix_decode_workspace_size")
 
 
 class SlmError(RuntimeError):
@@ -60,7 +60,9 @@ def load(path: Optional[str] = None):
         lib.slm_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.slm_shared_prefix_decode_attn.restype = ctypes.c_int
         lib.slm_shared_prefix_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
-                                                      f32, P, P, P, P, P, P]
+                                                      f32, P, P, P, P, P, P, sz, P]
+        lib.slm_shared_prefix_decode_workspace_size.restype = sz
+        lib.slm_shared_prefix_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.slm_beam_select.restype = ctypes.c_int
         lib.slm_beam_select.argtypes = [P, P, i32, i32, i32, P, P, P, P, P, P, P, P, sz, P]
         lib.slm_beam_select_workspace_size.restype = sz
@@ -118,6 +120,11 @@ def slm_beam_select_workspace_size(W_in: int, V: int, W: int) -> int:
     return int(load().slm_beam_select_workspace_size(W_in, V, W))
 
 
+def slm_shared_prefix_decode_workspace_size(W: int, Lp: int, n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
+    """Bytes of workspace that let the decode attention split the prompt's key blocks (0: never split)."""
+    return int(load().slm_shared_prefix_decode_workspace_size(W, Lp, n_q_heads, n_kv_heads, head_dim))
+
+
 def slm_abi_version() -> int:
     return int(load().slm_abi_version())
 
@@ -173,9 +180,13 @@ def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], v
                                   softmax_scale: Optional[float] = None, *, ks_out: torch.Tensor,
                                   vs_out: torch.Tensor, out: Optional[torch.Tensor] = None,
                                   lse: Optional[torch.Tensor] = None,
-                                  dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+                                  dev_status: Optional[torch.Tensor] = None,
+                                  workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
     """O [W, Hq, D] of beam decode attention over the shared prompt K/V plus
-    each beam's reordered suffix; writes the reordered suffix to ks_out/vs_out."""
+    each beam's reordered suffix; writes the reordered suffix to ks_out/vs_out.
+    ``workspace`` (uint8, device, zero-filled before its first use) lets the
+    prompt's key blocks be split over CTAs; when None a zeroed one of the size
+    the library asks for is allocated."""
     _need(q, "q", torch.bfloat16, 3)
     W, Hq, D = q.shape
     _need(ks_out, "ks_out", torch.bfloat16, 4)
@@ -206,10 +217,14 @@ def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], v
     _need(out, "out", torch.bfloat16, 3)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        n = slm_shared_prefix_decode_workspace_size(W, Lp, Hq, Hkv, D)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device) if n else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().slm_shared_prefix_decode_attn(
         _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(k_new), _ptr(v_new), _ptr(parent_idx), W, Lp,
         int(L_prev), Smax, Hq, Hkv, D, scale, _ptr(ks_out), _ptr(vs_out), _ptr(out), _ptr(lse), _ptr(dev_status),
-        _stream(q.device))
+        _ptr(workspace), ws_bytes, _stream(q.device))
     _check(st)
     return out
 

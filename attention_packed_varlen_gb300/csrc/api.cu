@@ -210,7 +210,7 @@ extern "C" {
 
 const char* slm_last_error(void) { return g_last_error.c_str(); }
 
-int32_t slm_abi_version(void) { return 1; }
+int32_t slm_abi_version(void) { return 2; }
 
 size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t n_q_heads,
                                   int32_t n_kv_heads) {
@@ -296,12 +296,35 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   return ok();
 }
 
+// Decode key-split workspace: the split parts of every output row (fp32 O and
+// (max, sum)), stored per sub-tile with rows innermost, and one ticket per
+// (beam tile pair, KV head, sub-tile).  The tickets must be zero before a
+// call; a call that completes leaves them zero.
+constexpr int64_t kMaxDecodeSplit = 16;
+struct DecodeSplitLayout {
+  size_t o_off, ml_off, ticket_off, ticket_bytes, total;
+};
+static DecodeSplitLayout decode_split_layout(int n_split, int W, int n_q_heads, int n_kv_heads, int head_dim) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const int tok = kBlockM / (n_q_heads / n_kv_heads);
+  const size_t tiles = static_cast<size_t>((W + 2 * tok - 1) / (2 * tok));
+  const size_t sub_tiles = tiles * n_kv_heads * 2;
+  DecodeSplitLayout l;
+  l.o_off = 0;
+  l.ml_off = up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * head_dim * sizeof(float));
+  l.ticket_off = l.ml_off + up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * 2 * sizeof(float));
+  l.ticket_bytes = sub_tiles * sizeof(int32_t);
+  l.total = l.ticket_off + up(l.ticket_bytes);
+  return l;
+}
+
 slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const void* vp, const void* ks,
                                          const void* vs, const void* k_new, const void* v_new,
                                          const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
                                          int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                          float softmax_scale, void* ks_out, void* vs_out, void* o, float* lse,
-                                         int32_t* dev_status, void* stream_) {
+                                         int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                         void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (W < 0 || Lp < 0 || L_prev < 0 || Smax < 0)
     return fail(SLM_ERR_INVALID_ARG, "negative size (W=%d Lp=%d L_prev=%d Smax=%d)", W, Lp, L_prev, Smax);
@@ -330,7 +353,27 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
   if (o == q) return fail(SLM_ERR_INVALID_ARG, "o aliases q");
 
   const int tok = kBlockM / G;
-  const int64_t n_units = static_cast<int64_t>((W + 2 * tok - 1) / (2 * tok)) * n_kv_heads;
+  const int64_t tiles = (W + 2 * tok - 1) / (2 * tok);
+  // Split the prompt's key blocks over CTAs when the tiles alone leave most
+  // SMs idle and the workspace has room for the split parts.
+  const int nb_all = (Lp + kBlockN - 1) / kBlockN;
+  int n_split = 1, blk_per_split = nb_all;
+  DecodeSplitLayout lay{};
+  if (workspace && nb_all > 1) {
+    const int64_t base = tiles * n_kv_heads;
+    const int want = static_cast<int>(std::min<int64_t>({static_cast<int64_t>(nb_all), kMaxDecodeSplit,
+                                                         std::max<int64_t>(1, num_sms() / base)}));
+    if (want > 1) {
+      const int bps = (nb_all + want - 1) / want;
+      const int ns = (nb_all + bps - 1) / bps;
+      lay = decode_split_layout(ns, W, n_q_heads, n_kv_heads, head_dim);
+      if (aligned16(workspace) && lay.total <= workspace_bytes) {
+        n_split = ns;
+        blk_per_split = bps;
+      }
+    }
+  }
+  const int64_t n_units = tiles * n_kv_heads * n_split;
   CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof tk);
   std::memset(&tv, 0, sizeof tv);
@@ -361,12 +404,30 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
   p.Lp = Lp;
   p.L_prev = L_prev;
   p.Smax = Smax;
+  p.n_split = n_split;
+  p.blk_per_split = blk_per_split;
+  if (n_split > 1) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.ws_o = reinterpret_cast<float*>(ws + lay.o_off);
+    p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml_off);
+    p.tickets = reinterpret_cast<int32_t*>(ws + lay.ticket_off);
+  }
   // decode writes O row by row (the suffix merge ends in registers); the
   // output map argument is unused
   cudaError_t e = (head_dim == 64) ? launch_attn<64, AttnMode::kDecodePrefix>(tq, tk, tv, tq, p, n_units, stream)
                                    : launch_attn<128, AttnMode::kDecodePrefix>(tq, tk, tv, tq, p, n_units, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   return ok();
+}
+
+size_t slm_shared_prefix_decode_workspace_size(int32_t W, int32_t Lp, int32_t n_q_heads, int32_t n_kv_heads,
+                                              int32_t head_dim) {
+  if (W <= 0 || Lp <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return 0;
+  if (head_dim != 64 && head_dim != 128) return 0;
+  const int nb_all = (Lp + kBlockN - 1) / kBlockN;
+  if (nb_all <= 1) return 0;
+  const int ns = static_cast<int>(std::min<int64_t>(nb_all, kMaxDecodeSplit));
+  return decode_split_layout(ns, W, n_q_heads, n_kv_heads, head_dim).total;
 }
 
 size_t slm_beam_select_workspace_size(int32_t W_in, int32_t V, int32_t W) {

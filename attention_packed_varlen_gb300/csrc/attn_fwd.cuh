@@ -67,6 +67,15 @@ struct AttnParams {
   __nv_bfloat16* ks_out;
   __nv_bfloat16* vs_out;
   int W, Lp, L_prev, Smax;
+  // decode with the prompt's key blocks split over CTAs: every split writes
+  // its rows' (max, sum, unnormalised O); the last split of a tile to finish
+  // merges them and runs the epilogue.  n_split = 1: no split.
+  // Parts are stored per sub-tile and column, rows innermost, so that the
+  // 128 threads of a sub-tile read and write them coalesced.
+  int n_split, blk_per_split;
+  float* ws_o;          // [n_split][tiles * n_kv_heads * 2][D][128]
+  float2* ws_ml;        // [n_split][tiles * n_kv_heads * 2][128]
+  int32_t* tickets;     // [tiles * n_kv_heads * 2]: zero between calls
 };
 
 template <int D>
@@ -100,12 +109,13 @@ struct UnitInfo {
   int n_tok[2];   // valid tokens / beams of each sub-tile
   int nblk[2];    // key blocks each sub-tile reads
   int nblk_max;
+  int tile, split;  // decode: beam tile pair and key split of the unit
 };
 
 template <AttnMode MODE>
 __device__ __forceinline__ int num_units(const AttnParams& p) {
   if constexpr (MODE == AttnMode::kPrefill) return p.items[0] * p.n_kv_heads;
-  else return ((p.W + 2 * p.tok_per_tile - 1) / (2 * p.tok_per_tile)) * p.n_kv_heads;
+  else return ((p.W + 2 * p.tok_per_tile - 1) / (2 * p.tok_per_tile)) * p.n_kv_heads * p.n_split;
 }
 
 // The memory part of a unit's description: the (start, length, pair) item
@@ -145,14 +155,20 @@ __device__ __forceinline__ UnitInfo unit_info(const AttnParams& p, int u, const 
       U.row0[t] = s0 + U.q0[t];
       U.nblk[t] = U.n_tok[t] > 0 ? (U.q0[t] + U.n_tok[t] + kBlockN - 1) / kBlockN : 0;
     }
+    U.tile = item;
+    U.split = 0;
   } else {
-    U.kv_begin = 0;
+    U.split = item % p.n_split;
+    U.tile = item / p.n_split;
+    const int b0 = U.split * p.blk_per_split;
+    const int nb = max(0, min(p.blk_per_split, (p.Lp + kBlockN - 1) / kBlockN - b0));
+    U.kv_begin = b0 * kBlockN;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       U.q0[t] = 0;
-      U.row0[t] = (2 * item + t) * TOK;
+      U.row0[t] = (2 * U.tile + t) * TOK;
       U.n_tok[t] = max(0, min(TOK, p.W - U.row0[t]));
-      U.nblk[t] = U.n_tok[t] > 0 ? (p.Lp + kBlockN - 1) / kBlockN : 0;
+      U.nblk[t] = U.n_tok[t] > 0 ? nb : 0;
     }
   }
   U.nblk_max = max(U.nblk[0], U.nblk[1]);
@@ -419,7 +435,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int key0 = j * kBlockN;
         int lim;
         if constexpr (MODE == AttnMode::kPrefill) lim = qpos - key0;
-        else lim = p.Lp - 1 - key0;
+        else lim = p.Lp - 1 - (U.kv_begin + key0);
         if (lim < kBlockN - 1) {
 #pragma unroll
           for (int c = 0; c < kBlockN; ++c)
@@ -470,13 +486,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before_sync();
         mbar_arrive(&bars[L::P_FULL + t]);
       }
-      if (!ok) break;
 
       // ---- epilogue ----
-      float acc[D];
-      if (U.nblk[t] > 0) {
+      // No warp leaves between a wait and the named barriers below: the four
+      // warps agree first (a warp whose wait gave up arrives with false; the
+      // others' waits then give up too, as the abort flag is set).
+      bool have_o = false;
+      if (ok && U.nblk[t] > 0) {
         ok = warp_wait(&bars[L::O_FULL + t], o_cnt & 1, abort_flag);
-        if (!ok) break;
+        have_o = ok;
+      }
+      __syncwarp();
+      ok = named_bar_and(1 + t, 128, ok);
+      if (!ok) break;
+      float acc[D];
+      if (have_o) {
         ++o_cnt;
         tc_fence_after_sync();
 #pragma unroll
@@ -497,6 +521,49 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int rowid = U.row0[t] + t_loc;  // token (prefill) or beam (decode)
 
       if constexpr (MODE == AttnMode::kDecodePrefix) {
+        if (p.n_split > 1) {
+          // This split's part of each row goes to the workspace; the last split
+          // of the sub-tile to arrive (ticket) merges all parts and goes on, the
+          // others are done.  The last one also sets the ticket back to zero.
+          const int64_t n_tt = static_cast<int64_t>((p.W + 2 * TOK - 1) / (2 * TOK)) * p.n_kv_heads * 2;
+          const int tt = (U.tile * p.n_kv_heads + U.kvh) * 2 + t;
+          {
+            float* dst = p.ws_o + (U.split * n_tt + tt) * D * 128 + r;
+#pragma unroll
+            for (int d = 0; d < D; ++d) __stcg(dst + d * 128, acc[d]);
+            __stcg(&p.ws_ml[(U.split * n_tt + tt) * 128 + r], make_float2(m_run, l_run));
+          }
+          __threadfence();
+          named_bar_sync(1 + t, 128);
+          volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 8 + 4 * t);
+          if (r == 0) {
+            const int last = atomicAdd(&p.tickets[tt], 1) == p.n_split - 1;
+            if (last) p.tickets[tt] = 0;  // no other split touches it in this call
+            *last_flag = last;
+          }
+          named_bar_sync(1 + t, 128);
+          if (!*last_flag) continue;
+          __threadfence();
+          if (row_valid) {
+            float m = m_run;
+            for (int s = 0; s < p.n_split; ++s)
+              if (s != U.split) m = fmaxf(m, __ldcg(&p.ws_ml[(s * n_tt + tt) * 128 + r]).x);
+            const float a = exp2_approx(m_run - m);
+            l_run *= a;
+#pragma unroll
+            for (int d = 0; d < D; ++d) acc[d] *= a;
+            for (int s = 0; s < p.n_split; ++s) {
+              if (s == U.split) continue;
+              const float2 ml = __ldcg(&p.ws_ml[(s * n_tt + tt) * 128 + r]);
+              const float f = exp2_approx(ml.x - m);
+              l_run = fmaf(ml.y, f, l_run);
+              const float* src = p.ws_o + (s * n_tt + tt) * D * 128 + r;
+#pragma unroll
+              for (int d = 0; d < D; ++d) acc[d] = fmaf(__ldcg(src + d * 128), f, acc[d]);
+            }
+            m_run = m;
+          }
+        }
         // Suffix keys of this beam on CUDA cores: its parent's history rows
         // then its own new row, merged into the same online-softmax state.
         if (row_valid) {

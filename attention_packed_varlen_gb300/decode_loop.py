@@ -45,6 +45,8 @@ class BeamDecodeLoop:
         if ws == 0:
             raise slm.SlmError(2, f"unsupported beam sizes W={W} V={V}")
         self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        dws = slm.slm_shared_prefix_decode_workspace_size(W, prefix_len, n_q_heads, n_kv_heads, head_dim)
+        self.dec_ws = torch.zeros(dws, dtype=torch.uint8, device=dev) if dws else None
         self.sel = []
         for t in range(n_steps + 1):
             w_in = 1 if t == 0 else W
@@ -101,7 +103,8 @@ class BeamDecodeLoop:
             prev = self.active(t - 1)
             slm.slm_shared_prefix_decode_attn(
                 q, kp, vp, self.ks[t - 1], self.vs[t - 1], k_new, v_new, prev["parent"], t - 1, self.scale,
-                ks_out=self.ks[t], vs_out=self.vs[t], out=self.o[t - 1], dev_status=self.status)
+                ks_out=self.ks[t], vs_out=self.vs[t], out=self.o[t - 1], dev_status=self.status,
+                workspace=self.dec_ws)
             self._select(t, logits, prev["score"])
             a = self.active(t)
             slm.slm_beam_reorder_history(self.hist[t - 1], a["parent"], a["token"], t, self.hist[t],

@@ -232,6 +232,8 @@ class BeamSet:
         self.o = torch.empty((W, Hq, D), dtype=torch.bfloat16, device=dev)
         from attention_packed_varlen_gb300 import _binding as slm
         self.ws = torch.empty(slm.slm_beam_select_workspace_size(W, bw.vocab, W), dtype=torch.uint8, device=dev)
+        dws = slm.slm_shared_prefix_decode_workspace_size(W, bw.prefix_len, Hq, Hkv, D)
+        self.dec_ws = torch.zeros(max(dws, 1), dtype=torch.uint8, device=dev)
         self.res = {
             "token": torch.empty(W, dtype=torch.int32, device=dev),
             "parent": torch.empty(W, dtype=torch.int32, device=dev),
@@ -265,7 +267,7 @@ def run_decode_step(slm_lib, bs: BeamSet, t: int, stream_ptr):
     st = slm_lib.slm_shared_prefix_decode_attn(
         P(q), P(bs.kp), P(bs.vp), P(ks_in), P(vs_in), P(kn), P(vn), P(parent), bw.beams, bw.prefix_len, t,
         bw.max_suffix, bw.n_q_heads, bw.n_kv_heads, bw.head_dim, bw.softmax_scale, P(ks_out), P(vs_out), P(bs.o),
-        None, None, stream_ptr)
+        None, None, P(bs.dec_ws), bs.dec_ws.numel(), stream_ptr)
     if st != 0:
         raise RuntimeError(slm_lib.slm_last_error().decode())
     r = bs.res

@@ -112,6 +112,18 @@ size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_
  *          state.  The prompt K/V is never reordered or copied.
  *   lse    (nullable) fp32 [W, Hq].
  *
+ *   workspace (nullable): device scratch, 16-byte aligned, of
+ *          workspace_bytes bytes, ZERO-FILLED before its first use.  With at
+ *          least slm_shared_prefix_decode_workspace_size(...) bytes the
+ *          prompt's key blocks may be split over several CTAs (their partial
+ *          softmax states merged before the suffix); with less, or NULL, they
+ *          are not split.  The result is the same up to fp32 summation order.
+ *          A call that completes leaves the workspace fit for the next call
+ *          (its tickets back at zero); after a call whose dev_status reports a
+ *          pipeline timeout, zero it again.  The caller owns the memory and
+ *          must not share it between calls in flight at the same time.
+ *   dev_status: nullable device int32 (bad parent index, pipeline timeout).
+ *
  * Requires Lp + L_s >= 1 and L_s <= Smax.
  */
 slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const void* vp, const void* ks,
@@ -119,7 +131,14 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
                                          const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
                                          int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                          float softmax_scale, void* ks_out, void* vs_out, void* o, float* lse,
-                                         int32_t* dev_status, void* stream);
+                                         int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                         void* stream);
+
+/* Workspace bytes that let slm_shared_prefix_decode_attn split the prompt's
+ * key blocks for these sizes (0 = it never splits them: Lp <= 128 or
+ * unsupported sizes). */
+size_t slm_shared_prefix_decode_workspace_size(int32_t W, int32_t Lp, int32_t n_q_heads, int32_t n_kv_heads,
+                                               int32_t head_dim);
 
 /*
  * Two-stage beam candidate selection (article section 3.3).

@@ -39,7 +39,7 @@ def test_header_declares_the_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} not exported"
-    assert lib.slm_abi_version() == 1
+    assert lib.slm_abi_version() == 2
     assert lib.slm_last_error() == b""
 
 
@@ -90,13 +90,13 @@ def _decode(lib, **kw):
     p = ctypes.c_void_p
     args = dict(q=p(16), kp=p(32), vp=p(48), ks=p(64), vs=p(80), kn=p(96), vn=p(112), parent=NULL, W=4, Lp=8,
                 L_prev=1, Smax=3, hq=14, hkv=2, d=64, scale=0.125, ks_out=p(128), vs_out=p(144), o=p(160),
-                lse=NULL, status=NULL, stream=NULL)
+                lse=NULL, status=NULL, ws=NULL, ws_bytes=0, stream=NULL)
     args.update(kw)
     a = args
     return lib.slm_shared_prefix_decode_attn(a["q"], a["kp"], a["vp"], a["ks"], a["vs"], a["kn"], a["vn"],
                                              a["parent"], a["W"], a["Lp"], a["L_prev"], a["Smax"], a["hq"],
                                              a["hkv"], a["d"], a["scale"], a["ks_out"], a["vs_out"], a["o"],
-                                             a["lse"], a["status"], a["stream"])
+                                             a["lse"], a["status"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 def test_decode_rejects_bad_arguments_on_host(lib):

@@ -30,7 +30,7 @@ def bits(t):
     return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True):
+def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True, workspace=None):
     dev = torch.device(DEV)
     W, Hq, D = d.q.shape
     Hkv = d.kp.shape[1] if d.kp is not None else d.k_new.shape[1]
@@ -44,7 +44,7 @@ def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True):
         d.q.to(dev), kp, vp, ks_dev, vs_dev,
         d.k_new.to(dev) if with_new else None, d.v_new.to(dev) if with_new else None,
         d.parent.to(dev) if parent else None, d.L_prev, d.softmax_scale,
-        ks_out=ks_out, vs_out=vs_out, lse=lse, dev_status=status)
+        ks_out=ks_out, vs_out=vs_out, lse=lse, dev_status=status, workspace=workspace)
     slm.slm_check_status(status)
     return o, lse, ks_out, vs_out
 
@@ -97,6 +97,27 @@ def test_decode_edge_cases(W, Lp, L_prev, Smax, hq, hkv, D, with_new, parent):
     dev = torch.device(DEV)
     o, lse, ks_out, vs_out = run_step(d, d.ks.to(dev), d.vs.to(dev), Smax, with_new=with_new, parent=parent)
     check_step(d, d.ks, d.vs, o, lse, ks_out, vs_out, f"W={W} Lp={Lp} L_prev={L_prev}", with_new, parent)
+
+
+@pytest.mark.parametrize("W,Lp,L_prev,hq,hkv,D", [
+    (400, 1024, 4, 14, 2, 64),     # the wide beam's last step: 8 key blocks over 24 tiles x heads
+    (37, 1000, 2, 4, 2, 128),      # head_dim 128, a ragged last key block
+    (5, 2000, 1, 8, 8, 64),        # MHA: more splits than the SMs need
+])
+def test_decode_key_split_matches_oracle_and_unsplit(W, Lp, L_prev, hq, hkv, D):
+    # the prompt's key blocks split over CTAs (workspace of the library's size) and
+    # not split (empty workspace) give the oracle's result; the two differ only by
+    # fp32 summation order
+    Smax = L_prev + 1
+    assert slm.slm_shared_prefix_decode_workspace_size(W, Lp, hq, hkv, D) > 0
+    d = wl.decode_inputs(W, Lp, L_prev, Smax, hq, hkv, D, seed=W * 7 + Lp)
+    dev = torch.device(DEV)
+    outs = {}
+    for name, ws in (("split", None), ("unsplit", torch.empty(0, dtype=torch.uint8, device=dev))):
+        o, lse, ks_out, vs_out = run_step(d, d.ks.to(dev), d.vs.to(dev), Smax, workspace=ws)
+        check_step(d, d.ks, d.vs, o, lse, ks_out, vs_out, f"{name} W={W} Lp={Lp}")
+        outs[name] = o.float()
+    assert (outs["split"] - outs["unsplit"]).abs().max().item() < 2e-2
 
 
 def test_decode_bad_parent_sets_device_status():
