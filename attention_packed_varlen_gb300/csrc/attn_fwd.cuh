@@ -486,21 +486,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before_sync();
         mbar_arrive(&bars[L::P_FULL + t]);
       }
+      if (!ok) break;
 
       // ---- epilogue ----
-      // No warp leaves between a wait and the named barriers below: the four
-      // warps agree first (a warp whose wait gave up arrives with false; the
-      // others' waits then give up too, as the abort flag is set).
-      bool have_o = false;
-      if (ok && U.nblk[t] > 0) {
-        ok = warp_wait(&bars[L::O_FULL + t], o_cnt & 1, abort_flag);
-        have_o = ok;
-      }
-      __syncwarp();
-      ok = named_bar_and(1 + t, 128, ok);
-      if (!ok) break;
       float acc[D];
-      if (have_o) {
+      if (U.nblk[t] > 0) {
+        ok = warp_wait(&bars[L::O_FULL + t], o_cnt & 1, abort_flag);
+        if (!ok) break;
         ++o_cnt;
         tc_fence_after_sync();
 #pragma unroll

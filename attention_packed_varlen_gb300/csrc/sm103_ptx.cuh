@@ -129,21 +129,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-// Named barrier that also ANDs a predicate over its threads: every thread
-// gets true only if all of them passed true.
-__device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
-
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (the tensor core reading an operand) after this fence.
 __device__ __forceinline__ void fence_proxy_async_smem() {
