@@ -162,7 +162,7 @@ class ClockSampler:
 # DRAM bytes (read + write) per prefill launch on this workload, from an ncu
 # capture of `bench.py --ncu-case prefill` (one layer of the same batch), keyed
 # by the kernel source it was taken on; any other source reports null.
-PREFILL_TRAFFIC = {"2f8683730f323e49": 1.166724e9 + 0.502974e9, "0723e93353cd1195": 1.238973e9 + 0.511833e9}
+PREFILL_TRAFFIC = {"c2b9e09bfb37964b": 1.231843e9 + 0.511996e9}
 
 
 def prefill_traffic():
@@ -556,7 +556,9 @@ def run_gpu(args):
 
     # e2e: the same prefill metric through the public API from pinned host
     # buffers: per layer, copy Q/K/V in, run, copy O out (one layer's host set
-    # reused for every layer)
+    # reused for every layer).  Copies in, attention and copies out run on
+    # three streams over two device buffer sets, so layer i+1's inputs arrive
+    # and layer i-1's output leaves while layer i computes.
     e2e = None
     if args.e2e_layers > 0:
         q0, k0, v0, _ = ps.layers[0]
@@ -567,16 +569,40 @@ def run_gpu(args):
         hq.copy_(q0)
         hk.copy_(k0)
         hv.copy_(v0)
-        dq, dk, dv, do = (torch.empty_like(q0), torch.empty_like(k0), torch.empty_like(v0), torch.empty_like(q0))
+        bufs = [(torch.empty_like(q0), torch.empty_like(k0), torch.empty_like(v0), torch.empty_like(q0))
+                for _ in range(2)]
+        s_in, s_run, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        sp_run = ctypes.c_void_p(s_run.cuda_stream)
+        ev = lambda: torch.cuda.Event()
+        loaded, ran, stored = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        used = [False, False]
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(args.e2e_layers):
-            dq.copy_(hq, non_blocking=True)
-            dk.copy_(hk, non_blocking=True)
-            dv.copy_(hv, non_blocking=True)
-            run_prefill_layer(lib, ps, (dq, dk, dv, do), sp)
-            ho.copy_(do, non_blocking=True)
+        for s_ in (s_in, s_run, s_out):
+            s_.wait_event(e0)
+        for i in range(args.e2e_layers):
+            b = i % 2
+            dq, dk, dv, do = bufs[b]
+            with torch.cuda.stream(s_in):
+                if used[b]:
+                    s_in.wait_event(ran[b])        # layer i-2 has read this set
+                dq.copy_(hq, non_blocking=True)
+                dk.copy_(hk, non_blocking=True)
+                dv.copy_(hv, non_blocking=True)
+                loaded[b].record(s_in)
+            s_run.wait_event(loaded[b])
+            if used[b]:
+                s_run.wait_event(stored[b])        # layer i-2's output has left
+            run_prefill_layer(lib, ps, (dq, dk, dv, do), sp_run)
+            ran[b].record(s_run)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ran[b])
+                ho.copy_(do, non_blocking=True)
+                stored[b].record(s_out)
+            used[b] = True
+        for s_ in (s_in, s_run, s_out):
+            stream.wait_stream(s_)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3)
