@@ -1172,7 +1172,10 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   e = cudaFuncSetAttribute(sel::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_sel));
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(sm_count());
+  // Narrow selections re-read a few hundred sub-chunks: 32 CTAs do it as fast
+  // as a CTA per SM and reach the last-CTA ranking sooner (measured 22.5 ->
+  // 21.9 us at W = 100); wide ones keep a CTA per SM.
+  cfg.gridDim = dim3(p.K <= 256 ? std::min(32, sm_count()) : sm_count());
   cfg.blockDim = dim3(sel::kSelThreads);
   cfg.dynamicSmemBytes = smem_sel;
   return cudaLaunchKernelEx(&cfg, sel::select_kernel, p);
