@@ -296,13 +296,16 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   return ok();
 }
 
-// Decode key-split workspace: the split parts of every output row (fp32 O and
-// (max, sum)), stored per sub-tile with rows innermost, and one ticket per
-// (beam tile pair, KV head, sub-tile).  The tickets must be zero before a
-// call; a call that completes leaves them zero.
+// Decode key-split workspace: a fixed area of tickets first (one per beam
+// tile pair, KV head and sub-tile; the same place whatever the call's sizes,
+// so no call's parts ever land on them), then the split parts of every output
+// row (fp32 O and (max, sum)), stored per sub-tile with rows innermost.  The
+// tickets must be zero before a call; a call that completes leaves them zero.
 constexpr int64_t kMaxDecodeSplit = 16;
+constexpr size_t kDecodeTickets = 4096;
 struct DecodeSplitLayout {
-  size_t o_off, ml_off, ticket_off, ticket_bytes, total;
+  size_t o_off, ml_off, ticket_off, total;
+  bool fits;  // the call's tickets fit the fixed area
 };
 static DecodeSplitLayout decode_split_layout(int n_split, int W, int n_q_heads, int n_kv_heads, int head_dim) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
@@ -310,11 +313,11 @@ static DecodeSplitLayout decode_split_layout(int n_split, int W, int n_q_heads, 
   const size_t tiles = static_cast<size_t>((W + 2 * tok - 1) / (2 * tok));
   const size_t sub_tiles = tiles * n_kv_heads * 2;
   DecodeSplitLayout l;
-  l.o_off = 0;
-  l.ml_off = up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * head_dim * sizeof(float));
-  l.ticket_off = l.ml_off + up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * 2 * sizeof(float));
-  l.ticket_bytes = sub_tiles * sizeof(int32_t);
-  l.total = l.ticket_off + up(l.ticket_bytes);
+  l.ticket_off = 0;
+  l.o_off = kDecodeTickets * sizeof(int32_t);
+  l.ml_off = l.o_off + up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * head_dim * sizeof(float));
+  l.total = l.ml_off + up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * 2 * sizeof(float));
+  l.fits = sub_tiles <= kDecodeTickets;
   return l;
 }
 
@@ -367,7 +370,7 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
       const int bps = (nb_all + want - 1) / want;
       const int ns = (nb_all + bps - 1) / bps;
       lay = decode_split_layout(ns, W, n_q_heads, n_kv_heads, head_dim);
-      if (aligned16(workspace) && lay.total <= workspace_bytes) {
+      if (lay.fits && aligned16(workspace) && lay.total <= workspace_bytes) {
         n_split = ns;
         blk_per_split = bps;
       }

@@ -118,9 +118,9 @@ size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_
  *          prompt's key blocks may be split over several CTAs (their partial
  *          softmax states merged before the suffix); with less, or NULL, they
  *          are not split.  The result is the same up to fp32 summation order.
- *          A call that completes leaves the workspace fit for the next call
- *          (its tickets back at zero); after a call whose dev_status reports a
- *          pipeline timeout, zero it again.  The caller owns the memory and
+ *          A call that completes leaves the workspace fit for the next call,
+ *          of any sizes (its tickets back at zero); after a call whose
+ *          dev_status reports a pipeline timeout, zero it again.  The caller owns the memory and
  *          must not share it between calls in flight at the same time.
  *   dev_status: nullable device int32 (bad parent index, pipeline timeout).
  *

@@ -54,6 +54,17 @@ def test_workspace_size_queries(lib):
     assert _binding.slm_beam_select_workspace_size(400, 151936, 400) > 0
     assert _binding.slm_beam_select_workspace_size(1, 151936, 400) > 0
     assert _binding.slm_beam_select_workspace_size(4, 10, 6) == 0           # 2W > V
+    # decode key split: nothing to split in one key block of 128 rows
+    assert _binding.slm_shared_prefix_decode_workspace_size(100, 96, 14, 2, 64) == 0
+    assert _binding.slm_shared_prefix_decode_workspace_size(100, 128, 14, 2, 64) == 0
+    assert _binding.slm_shared_prefix_decode_workspace_size(100, 1024, 14, 13, 64) == 0  # Hq % Hkv != 0
+    assert _binding.slm_shared_prefix_decode_workspace_size(100, 1024, 14, 2, 80) == 0   # head_dim
+    # W=400, Lp=1024, 14q/2kv, D=64: up to 8 splits x 48 sub-tiles x 128 rows x (64 fp32 + (max, sum))
+    n = _binding.slm_shared_prefix_decode_workspace_size(400, 1024, 14, 2, 64)
+    assert n >= 8 * 48 * 128 * (64 * 4 + 8) + 48 * 4 and n % 256 == 0
+    # more key blocks or more beams never need less
+    assert _binding.slm_shared_prefix_decode_workspace_size(400, 2048, 14, 2, 64) >= n
+    assert _binding.slm_shared_prefix_decode_workspace_size(800, 1024, 14, 2, 64) >= n
 
 
 NULL = None

@@ -120,6 +120,21 @@ def test_decode_key_split_matches_oracle_and_unsplit(W, Lp, L_prev, hq, hkv, D):
     assert (outs["split"] - outs["unsplit"]).abs().max().item() < 2e-2
 
 
+def test_decode_workspace_serves_calls_of_other_shapes_and_too_small_runs_unsplit():
+    # one zero-filled workspace, sized for the widest call, serves calls of other
+    # shapes in turn (a completed call leaves its tickets at zero again); a
+    # workspace far too small is ignored and the call runs unsplit
+    dev = torch.device(DEV)
+    ws = torch.zeros(slm.slm_shared_prefix_decode_workspace_size(400, 1024, 14, 2, 64), dtype=torch.uint8,
+                     device=dev)
+    tiny = torch.zeros(256, dtype=torch.uint8, device=dev)
+    for i, (W, Lp, L_prev, w) in enumerate(((400, 1024, 2, ws), (37, 300, 1, ws), (400, 1024, 0, ws),
+                                             (130, 600, 3, ws), (400, 1024, 1, tiny))):
+        d = wl.decode_inputs(W, Lp, L_prev, L_prev + 1, 14, 2, 64, seed=100 + i)
+        o, lse, ks_out, vs_out = run_step(d, d.ks.to(dev), d.vs.to(dev), L_prev + 1, workspace=w)
+        check_step(d, d.ks, d.vs, o, lse, ks_out, vs_out, f"call {i}: W={W} Lp={Lp} L_prev={L_prev}")
+
+
 def test_decode_bad_parent_sets_device_status():
     d = wl.decode_inputs(8, 32, 1, 3, 14, 2, 64, seed=3)
     dev = torch.device(DEV)
