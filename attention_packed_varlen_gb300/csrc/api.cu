@@ -114,8 +114,19 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), max_units)));
-  kern<<<grid, kFwdThreads, smem, stream>>>(tq, tk, tv, to, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFwdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if constexpr (MODE == AttnMode::kPrefill) {  // overlaps the schedule kernel launched just before
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p);
 }
 
 // ---- prefill tile schedule -------------------------------------------------
@@ -134,11 +145,26 @@ __global__ void __launch_bounds__(kSchedThreads)
   __shared__ int cnt[kBuckets];
   __shared__ int warp_tot[kSchedThreads / 32];
   __shared__ int bad;
+  pdl_launch_dependents();  // the attention kernel may start its setup now
+  // the first kSchedThreads sequences' boundaries, loaded once
+  const int b_own = threadIdx.x;
+  const int s0_own = (b_own < B) ? cu[b_own] : 0;
+  const int len_own = (b_own < B) ? cu[b_own + 1] - s0_own : 0;
+  auto seq = [&](int b, int& s0, int& len) {
+    if (b == b_own) {
+      s0 = s0_own;
+      len = len_own;
+    } else {
+      s0 = cu[b];
+      len = cu[b + 1] - s0;
+    }
+  };
   for (int i = threadIdx.x; i < kBuckets; i += kSchedThreads) cnt[i] = 0;
   if (threadIdx.x == 0) bad = (cu[0] != 0 || cu[B] != T) ? 1 : 0;
   __syncthreads();
   for (int b = threadIdx.x; b < B; b += kSchedThreads) {
-    const int len = cu[b + 1] - cu[b];
+    int s0, len;
+    seq(b, s0, len);
     if (len < 0 || (len + kBlockN - 1) / kBlockN > max_nb) bad = 1;
   }
   __syncthreads();
@@ -150,7 +176,8 @@ __global__ void __launch_bounds__(kSchedThreads)
     return;
   }
   for (int b = threadIdx.x; b < B; b += kSchedThreads) {
-    const int len = cu[b + 1] - cu[b];
+    int s0, len;
+    seq(b, s0, len);
     if (len > 0) atomicAdd(&cnt[(len + kBlockN - 1) / kBlockN], (len + tok2 - 1) / tok2);
   }
   __syncthreads();
@@ -182,11 +209,11 @@ __global__ void __launch_bounds__(kSchedThreads)
   }
   __syncthreads();
   for (int b = threadIdx.x; b < B; b += kSchedThreads) {
-    const int len = cu[b + 1] - cu[b];
+    int s0, len;
+    seq(b, s0, len);
     if (len <= 0) continue;
     const int n_items = (len + tok2 - 1) / tok2;
     const int pos = atomicAdd(&cnt[(len + kBlockN - 1) / kBlockN], n_items);
-    const int s0 = cu[b];
     for (int k = 0; k < n_items; ++k) {
       items[1 + 3 * (pos + k)] = s0;
       items[2 + 3 * (pos + k)] = len;

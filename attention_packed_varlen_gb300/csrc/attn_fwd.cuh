@@ -197,8 +197,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int G = p.group;
   const int TOK = p.tok_per_tile;
   const int rows_used = TOK * G;
-  const int n_units = num_units<MODE>(p);
-  if (static_cast<int>(blockIdx.x) >= n_units) return;
 
   auto q_tile = [&](int qb, int t) { return smem + L::kQ + (qb * 2 + t) * L::kTile; };
   auto kv_tile = [&](uint32_t slot) { return smem + L::kKV + slot * L::kTile; };
@@ -253,6 +251,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Prefill runs as a programmatic dependent of its schedule kernel: the
+  // setup above overlaps it, the work items are read only after this.  A CTA
+  // beyond the last unit runs empty loops and frees its TMEM.
+  pdl_wait();
+  const int n_units = num_units<MODE>(p);
 
   if (warp == 8) {
     // ======================= TMA producer =======================

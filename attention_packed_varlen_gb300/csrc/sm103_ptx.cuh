@@ -107,6 +107,13 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
+// Programmatic dependent launch: a dependent grid may start once every CTA
+// of this grid has called launch_dependents (or exited); its wait returns
+// when this grid has completed and its memory is visible.  The wait returns
+// at once in a grid that was not launched as a dependent.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // 3-D tiled store shared -> global (bulk async-group); same coordinate rules
 // as the load, never at negative coordinates.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int c0, int c1, int c2) {
