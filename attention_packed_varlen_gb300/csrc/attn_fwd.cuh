@@ -197,6 +197,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int G = p.group;
   const int TOK = p.tok_per_tile;
   const int rows_used = TOK * G;
+  // decode: the units are known from the arguments; CTAs beyond them leave
+  const int n_units_dec = (MODE == AttnMode::kPrefill) ? 0 : num_units<MODE>(p);
+  if (MODE != AttnMode::kPrefill && static_cast<int>(blockIdx.x) >= n_units_dec) return;
 
   auto q_tile = [&](int qb, int t) { return smem + L::kQ + (qb * 2 + t) * L::kTile; };
   auto kv_tile = [&](uint32_t slot) { return smem + L::kKV + slot * L::kTile; };
@@ -254,8 +257,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   // Prefill runs as a programmatic dependent of its schedule kernel: the
   // setup above overlaps it, the work items are read only after this.  A CTA
   // beyond the last unit runs empty loops and frees its TMEM.
-  pdl_wait();
-  const int n_units = num_units<MODE>(p);
+  if constexpr (MODE == AttnMode::kPrefill) pdl_wait();
+  const int n_units = (MODE == AttnMode::kPrefill) ? num_units<MODE>(p) : n_units_dec;
 
   if (warp == 8) {
     // ======================= TMA producer =======================
