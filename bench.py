@@ -162,7 +162,7 @@ class ClockSampler:
 # DRAM bytes (read + write) per prefill launch on this workload, from an ncu
 # capture of `bench.py --ncu-case prefill` (one layer of the same batch), keyed
 # by the kernel source it was taken on; any other source reports null.
-PREFILL_TRAFFIC = {"c2b9e09bfb37964b": 1.231843e9 + 0.511996e9}
+PREFILL_TRAFFIC = {"54baa8a268212bb2": 1.221418e9 + 0.512403e9}
 
 
 def prefill_traffic():
