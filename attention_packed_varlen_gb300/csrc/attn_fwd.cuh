@@ -12,8 +12,9 @@
 // Warp roles (320 threads):
 //   warps 0-3  softmax of sub-tile 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax of sub-tile 1
-//   warp  8    TMA producer: lane 1 loads Q tiles (double-buffered across
-//              units), lane 0 a ring of K/V blocks, 128-byte swizzled
+//   warp  8    TMA producer: lane 1 loads Q tiles (two buffers across units
+//              at D = 64, one at D = 128), lane 0 a ring of K/V blocks,
+//              128-byte swizzled
 //   warp  9    tcgen05 issuer: S_t = Q_t K^T into TMEM, then O_t += P_t V
 //              with P_t read back from TMEM where the softmax wrote it over
 //              S_t (bf16, two per column)
@@ -24,6 +25,12 @@
 // PV_t(j) is done and may rescale O_t.  The online softmax keeps its running
 // maximum until a block raises it by more than 2^8 (the factor cancels in the
 // final division), so O is rarely rescaled.
+//
+// Prefill runs as a programmatic dependent of its schedule kernel (setup
+// first, griddepcontrol.wait before the work items are read).  Decode can
+// split the prompt's key blocks over several CTAs per beam tile: each split
+// leaves its rows' partial softmax state in a caller workspace and the last
+// one to finish (atomic ticket) merges them before the suffix keys.
 //
 // Every mbarrier wait is bounded (see sm103_ptx.cuh); a stuck pipeline ends
 // the kernel with a status bit instead of a hang.

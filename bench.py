@@ -161,19 +161,29 @@ class ClockSampler:
 
 # DRAM bytes (read + write) per prefill launch on this workload, from an ncu
 # capture of `bench.py --ncu-case prefill` (one layer of the same batch), keyed
-# by the kernel source it was taken on; any other source reports null.
-PREFILL_TRAFFIC = {"54baa8a268212bb2": 1.221418e9 + 0.512403e9}
+# by the code it was taken on (the kernel, its PTX helpers and the host launch,
+# comments and blank space left out); any other code reports null.
+PREFILL_TRAFFIC = {"fad776abb630d9de": 1.221418e9 + 0.512403e9}
+
+
+def prefill_code_key() -> str:
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for name in ("attn_fwd.cuh", "sm103_ptx.cuh", "api.cu"):
+        with open(os.path.join(ROOT, "attention_packed_varlen_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
+    return h.hexdigest()[:16]
 
 
 def prefill_traffic():
-    import hashlib
-    path = os.path.join(ROOT, "attention_packed_varlen_gb300", "csrc", "attn_fwd.cuh")
     try:
-        with open(path, "rb") as f:
-            key = hashlib.sha256(f.read()).hexdigest()[:16]
+        return PREFILL_TRAFFIC.get(prefill_code_key())
     except OSError:
         return None
-    return PREFILL_TRAFFIC.get(key)
 
 
 # ----------------------------------------------------------------------------
