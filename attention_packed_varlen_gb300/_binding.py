@@ -173,6 +173,20 @@ def slm_packed_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, c
 # ----------------------------------------------------------------------------
 # Shared-prefix decode
 # ----------------------------------------------------------------------------
+_decode_ws = {}  # (device, stream) -> zero-filled decode workspace, grown on demand
+
+
+def _decode_workspace(device: torch.device, n: int) -> torch.Tensor:
+    if torch.cuda.is_current_stream_capturing():  # never keep memory of a graph's private pool
+        return torch.zeros(n, dtype=torch.uint8, device=device)
+    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _decode_ws.get(key)
+    if ws is None or ws.numel() < n:
+        ws = torch.zeros(n, dtype=torch.uint8, device=device)
+        _decode_ws[key] = ws
+    return ws
+
+
 def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], vp: Optional[torch.Tensor],
                                   ks: Optional[torch.Tensor], vs: Optional[torch.Tensor],
                                   k_new: Optional[torch.Tensor], v_new: Optional[torch.Tensor],
@@ -185,8 +199,9 @@ def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], v
     """O [W, Hq, D] of beam decode attention over the shared prompt K/V plus
     each beam's reordered suffix; writes the reordered suffix to ks_out/vs_out.
     ``workspace`` (uint8, device, zero-filled before its first use) lets the
-    prompt's key blocks be split over CTAs; when None a zeroed one of the size
-    the library asks for is allocated."""
+    prompt's key blocks be split over CTAs; when None, a zeroed one kept per
+    device and stream is used (a completed call leaves it fit for the next;
+    inside a CUDA graph capture a fresh one is allocated instead)."""
     _need(q, "q", torch.bfloat16, 3)
     W, Hq, D = q.shape
     _need(ks_out, "ks_out", torch.bfloat16, 4)
@@ -219,7 +234,7 @@ def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], v
         _need(lse, "lse", torch.float32, 2)
     if workspace is None:
         n = slm_shared_prefix_decode_workspace_size(W, Lp, Hq, Hkv, D)
-        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device) if n else None
+        workspace = _decode_workspace(q.device, n) if n else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     st = load().slm_shared_prefix_decode_attn(
         _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(k_new), _ptr(v_new), _ptr(parent_idx), W, Lp,
