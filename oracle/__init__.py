@@ -171,18 +171,28 @@ def row_lse(logits) -> np.ndarray:
     return out
 
 
-def beam_select(logits, cum_scores, n_keep: int):
+def beam_select(logits, cum_scores, n_keep: int, lse_in=None):
     """Full sort of all W_in x V candidates; returns the first ``n_keep`` as
-    (token int32, parent int32, score fp32, lse fp32 [W_in])."""
+    (token int32, parent int32, score fp32, lse fp32 [W_in]).
+
+    ``lse_in`` (fp32 [W_in], optional) replaces the oracle's own row
+    log-normalisers: the ranking is then that of the same scores formed from
+    the given normalisers (used to check a selection given its own fp32
+    log-softmax)."""
     lib = _load()
     lb = _bits(logits)
     W_in, V = lb.shape
     cum = np.ascontiguousarray(np.asarray(cum_scores, dtype=np.float32))
+    lse_given = None
+    if lse_in is not None:
+        lse_given = np.ascontiguousarray(np.asarray(lse_in, dtype=np.float32))
+        if lse_given.shape != (W_in,):
+            raise ValueError("lse_in must have one value per row")
     tok = np.zeros((n_keep,), dtype=np.int32)
     par = np.zeros((n_keep,), dtype=np.int32)
     sc = np.zeros((n_keep,), dtype=np.float32)
     lse = np.zeros((W_in,), dtype=np.float32)
-    rc = lib.oracle_beam_select(_ptr(lb), _ptr(cum), W_in, V, int(n_keep), None,
+    rc = lib.oracle_beam_select(_ptr(lb), _ptr(cum), W_in, V, int(n_keep), _ptr(lse_given),
                                 _ptr(tok), _ptr(par), _ptr(sc), _ptr(lse))
     if rc == -2:
         raise MemoryError("oracle_beam_select could not allocate its sort buffer")

@@ -163,6 +163,19 @@ def reorder_history(hist_in, parent, token, t: int):
     return out
 
 
+def candidate_scores(logits, cum, lse, parent, token) -> np.ndarray:
+    """fp32 scores of the given (parent, token) candidates, formed as the
+    article's section 3.3 fixes them: fl32(cum[p] + fl32(x[p, v] - lse[p]))
+    with x the bf16 logit widened exactly and lse the fp32 log-normaliser."""
+    import oracle as _o
+    bits = _o._bits(logits)
+    par = np.asarray(parent, dtype=np.int64)
+    tok = np.asarray(token, dtype=np.int64)
+    x = (bits[par, tok].astype(np.uint32) << 16).view(np.float32)
+    lp = (x - np.asarray(lse, dtype=np.float32)[par]).astype(np.float32)
+    return (np.asarray(cum, dtype=np.float32)[par] + lp).astype(np.float32)
+
+
 def beam_decode_loop(logits0, kp, vp, steps, W: int, softmax_scale: float, stop_id=None, follow=None,
                      n_threads: int = 1):
     """Fixed-depth beam search (section 2.3), one record per step.
@@ -179,17 +192,20 @@ def beam_decode_loop(logits0, kp, vp, steps, W: int, softmax_scale: float, stop_
       3. with a stop id, sets finished hypotheses aside (``split_finished``);
       4. reorders the token history by the new parents (``reorder_history``).
 
-    Each record holds ``cand`` = (token, parent, score, lse) of the top 2W,
+    Each record holds ``cum`` (the cumulative scores the step's selection
+    started from), ``cand`` = (token, parent, score, lse) of the top 2W,
     ``active`` = (token, parent, score) of the W beams that go on,
     ``finished`` (list of (token, parent, score)), ``hist`` [W, t+1] and, for
     t >= 1, the attention ``o``, ``lse`` and reordered suffix ``ks``/``vs``
     (bf16 bits) of that step.
 
-    ``follow(t, rec)``, when given, returns the (token, parent, score) arrays
-    to go on with after step t instead of the record's own -- e.g. those of
-    another run whose near-equal scores were ordered differently -- so that
-    every later step is compared on the same beams.  The hypotheses ``hist``
-    and ``ks``/``vs`` follow the same beams."""
+    ``follow(t, rec)``, when given, returns the (token, parent) arrays of the
+    beams to go on with after step t instead of the record's own -- e.g.
+    those of another run whose near-equal scores were ordered differently --
+    so that every later step is compared on the same beams.  Only the beams'
+    identity is taken: their cumulative scores are this oracle's own,
+    ``candidate_scores`` from its own log-normalisers and its own earlier
+    scores.  The hypotheses ``hist`` and ``ks``/``vs`` follow the same beams."""
     import oracle as _o  # the package's C-backed attention and selection
 
     def split(tok, par, sc):
@@ -199,17 +215,20 @@ def beam_decode_loop(logits0, kp, vp, steps, W: int, softmax_scale: float, stop_
         return (np.array([a[0] for a in act], np.int32), np.array([a[1] for a in act], np.int32),
                 np.array([a[2] for a in act], np.float32)), fin
 
-    def go_on(t, rec):
+    def go_on(t, rec, logits, cum):
         if follow is None:
             return rec["active"]
-        a = follow(t, rec)
-        return (np.asarray(a[0], np.int32), np.asarray(a[1], np.int32), np.asarray(a[2], np.float32))
+        tok, par = follow(t, rec)
+        tok = np.asarray(tok, np.int32)
+        par = np.asarray(par, np.int32)
+        return tok, par, candidate_scores(logits, cum, rec["cand"][3], par, tok)
 
     recs = []
-    cand = _o.beam_select(logits0, np.zeros(1, np.float32), 2 * W)
+    cum = np.zeros(1, np.float32)
+    cand = _o.beam_select(logits0, cum, 2 * W)
     active, fin = split(*cand[:3])
-    rec = {"cand": cand, "active": active, "finished": fin}
-    state = go_on(0, rec)
+    rec = {"cum": cum, "cand": cand, "active": active, "finished": fin}
+    state = go_on(0, rec, logits0, cum)
     rec["hist"] = reorder_history(None, None, state[0], 0)
     recs.append(rec)
     hist = rec["hist"]
@@ -222,10 +241,12 @@ def beam_decode_loop(logits0, kp, vp, steps, W: int, softmax_scale: float, stop_
         parent = state[1]
         o, lse, ks, vs = _o.shared_prefix_decode(q, kp, vp, ks, vs, k_new, v_new, parent, t - 1, softmax_scale,
                                                  n_threads=n_threads)
-        cand = _o.beam_select(logits, state[2], 2 * W)
+        cum = state[2]
+        cand = _o.beam_select(logits, cum, 2 * W)
         active, fin = split(*cand[:3])
-        rec = {"cand": cand, "active": active, "finished": fin, "o": o, "lse": lse, "ks": ks, "vs": vs}
-        state = go_on(t, rec)
+        rec = {"cum": cum, "cand": cand, "active": active, "finished": fin, "o": o, "lse": lse, "ks": ks,
+               "vs": vs}
+        state = go_on(t, rec, logits, cum)
         hist = reorder_history(hist, state[1], state[0], t)
         rec["hist"] = hist
         recs.append(rec)

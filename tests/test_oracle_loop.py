@@ -126,9 +126,9 @@ def test_follow_replaces_the_kept_set():
     own = H.beam_decode_loop(d.logits0, d.kp, d.vp, d.steps, W, SCALE)
 
     def swap_first_two(t, rec):
-        tok, par, sc = (a.copy() for a in rec["active"])
-        tok[[0, 1]], par[[0, 1]], sc[[0, 1]] = tok[[1, 0]], par[[1, 0]], sc[[1, 0]]
-        return tok, par, sc
+        tok, par = (a.copy() for a in rec["active"][:2])
+        tok[[0, 1]], par[[0, 1]] = tok[[1, 0]], par[[1, 0]]
+        return tok, par
 
     fol = H.beam_decode_loop(d.logits0, d.kp, d.vp, d.steps, W, SCALE, follow=swap_first_two)
     assert fol[0]["hist"][0].tolist() == own[0]["hist"][1].tolist()
@@ -138,3 +138,41 @@ def test_follow_replaces_the_kept_set():
     k1 = d.steps[0][1].view(torch.int16).numpy().view(np.uint16)
     for b in range(W):
         np.testing.assert_array_equal(fol[2]["ks"][b, 0], k1[par[b]])
+
+
+def test_following_its_own_beams_changes_nothing():
+    # follow() hands over only the beams' identity; the loop then scores them
+    # itself.  Following its own kept beams must give every record bit for
+    # bit, so the followed scores are the same fp32 arithmetic as the sort's.
+    for seed, stop in ((6, None), (7, 7)):
+        d = tiny(seed, stop_id=stop, stop_rows=0.5 if stop is not None else 0.0)
+        own = H.beam_decode_loop(d.logits0, d.kp, d.vp, d.steps, W, SCALE, stop_id=stop)
+        fol = H.beam_decode_loop(d.logits0, d.kp, d.vp, d.steps, W, SCALE, stop_id=stop,
+                                 follow=lambda t, rec: rec["active"][:2])
+        for a, b in zip(own, fol):
+            for k in ("cum", "hist"):
+                np.testing.assert_array_equal(a[k], b[k])
+            for x, y in zip(a["cand"], b["cand"]):
+                np.testing.assert_array_equal(np.asarray(x).view(np.int32), np.asarray(y).view(np.int32))
+
+
+def test_followed_beams_are_scored_by_the_oracle():
+    # a followed beam that the oracle itself did not keep gets the oracle's
+    # own score for it: its cumulative score plus its fp32 log-probability
+    d = tiny(8)
+    last = {}
+
+    def take_third_candidate(t, rec):
+        tok, par = (a.copy() for a in rec["active"][:2])
+        tok[0], par[0] = rec["cand"][0][W], rec["cand"][1][W]   # rank W: not kept by the oracle
+        last[t] = (tok, par)
+        return tok, par
+
+    fol = H.beam_decode_loop(d.logits0, d.kp, d.vp, d.steps, W, SCALE, follow=take_third_candidate)
+    for t in range(1, len(fol)):
+        tok, par = last[t - 1]
+        x = f64(d.logits0 if t == 1 else d.steps[t - 2][3])
+        prev_cum = fol[t - 1]["cum"]
+        lse = logsoftmax(x)
+        want = np.asarray(prev_cum, np.float64)[par] + lse[par, tok]
+        np.testing.assert_allclose(fol[t]["cum"], want, rtol=0, atol=1e-5)

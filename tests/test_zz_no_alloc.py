@@ -7,8 +7,10 @@ keeps its tile schedule in a fixed array of the library's own device memory.
 The test calls it through the C ABI twice in a row, on different inputs, and
 checks each output against the workspace entry point slm_packed_prefill_attn
 on the same inputs, within the attention tolerance of the parity tests (the
-two run the same kernels, so they are expected to agree exactly).  It also
-checks that a request too large for the built-in array is refused cleanly.
+two run the same kernels, so they are expected to agree exactly), and against
+the CPU oracle, so that a fault in the schedule both share cannot pass.  It
+also checks that a request too large for the built-in array is refused
+cleanly.
 The file name makes pytest collect it last.
 """
 import ctypes
@@ -17,8 +19,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from attention_packed_varlen_gb300 import _binding as slm
 from attention_packed_varlen_gb300 import build, workloads as wl
+from tests.parity import check_attention, check_lse
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -61,6 +65,10 @@ def test_noalloc_prefill_matches_workspace_entry_point(lib):
         err = np.abs(a - b)
         assert err.max() <= 1e-2 and err.mean() <= 1e-3, (err.max(), err.mean())
         assert np.abs(lse.cpu().numpy() - ref_lse.cpu().numpy()).max() <= 1e-4
+        o_ref, lse_ref = oracle.packed_prefill(inp.q, inp.k, inp.v, inp.cu_seqlens.numpy(), inp.softmax_scale,
+                                               want_lse=True, n_threads=oracle.default_threads())
+        check_attention(out.cpu(), o_ref, "no-allocation entry point vs oracle")
+        check_lse(lse.cpu(), lse_ref, "no-allocation entry point vs oracle")
 
 
 def test_noalloc_prefill_refuses_requests_beyond_its_buffer(lib):
