@@ -37,6 +37,8 @@ MISTAKES = {
     "parent tie rule reversed": ("if (a->b != c->b) return a->b < c->b ? -1 : 1;",
                                  "if (a->b != c->b) return a->b > c->b ? -1 : 1;"),
     "log-normaliser without the sum": ("lse_out[b] = (float)(m + log(s));", "lse_out[b] = (float)(m);"),
+    "logit tie rule reversed": ("if (a->x > c->x) return -1;", "if (a->x < c->x) return -1;"),
+    "logit tie key dropped": ("if (a->x > c->x) return -1;\n    if (a->x < c->x) return 1;\n", ""),
 }
 
 PIN_FILES = ["test_oracle_prefill.py", "test_oracle_decode.py", "test_oracle_select.py"]

@@ -114,6 +114,24 @@ def test_two_stage_pruning_with_ties():
     np.testing.assert_array_equal(par, p2[:2 * W])
 
 
+def test_two_stage_orders_equal_scores_by_logit():
+    # Distinct bf16 logits whose fp32 log-probabilities round to one value
+    # (all below half an fp32 ulp of the row's lse = ln 4): their scores tie
+    # exactly, and the article's per-beam Top-K on the logits (section 3.3)
+    # puts the higher logit first even when it has the higher token id.
+    V, W = 16, 2
+    x = torch.full((2, V), -30.0)
+    x[:, :4] = torch.tensor([0.0, 2.0 ** -27, 2.0 ** -26, 2.0 ** -25])
+    logits = x.to(torch.bfloat16)
+    cum = torch.tensor([0.0, -1.0])
+    tok, par, sc, lse = oracle.beam_select(logits, cum, 2 * W)
+    assert len(set(sc[:4].tolist())) == 1, "the case needs four exactly tied scores"
+    t2, p2, _ = two_stage_select(logits, cum, W, lse)
+    np.testing.assert_array_equal(tok, t2[:2 * W])
+    np.testing.assert_array_equal(par, p2[:2 * W])
+    assert tok.tolist() == [3, 2, 1, 0]
+
+
 def test_ids_from_logits_equal_ids_from_log_probs():
     # article, section 3.3: log-softmax is strictly monotone within a row, so
     # Top-K on bf16 logits and on fp64 log-probabilities pick the same ids
