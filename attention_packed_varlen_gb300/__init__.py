@@ -15,7 +15,10 @@ from ._binding import (  # noqa: F401
     slm_beam_select_workspace_size,
     slm_check_status,
     slm_packed_prefill_attn,
+    slm_packed_prefill_attn_f32,
     slm_prefill_workspace_size,
+    slm_set_wait_timeout_ns,
     slm_shared_prefix_decode_attn,
+    slm_shared_prefix_decode_attn_f32,
     slm_shared_prefix_decode_workspace_size,
 )

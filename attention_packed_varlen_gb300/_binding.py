@@ -25,7 +25,8 @@ STATUS_NAMES = {0: "SLM_OK", 1: "SLM_ERR_INVALID_ARG", 2: "SLM_ERR_UNSUPPORTED",
 EXPORTS = ("slm_last_error", "slm_abi_version", "slm_packed_prefill_attn", "slm_prefill_workspace_size",
            "slm_shared_prefix_decode_attn", "slm_beam_select", "slm_beam_select_workspace_size",
            "slm_check_status", "slm_packed_prefill_attn_noalloc", "slm_swiglu_quant_e4m3", "slm_label_scores",
-           "slm_beam_split_finished", "slm_beam_reorder_history", "slm_shared_prefix_decode_workspace_size")
+           "slm_beam_split_finished", "slm_beam_reorder_history", "slm_shared_prefix_decode_workspace_size",
+           "slm_packed_prefill_attn_f32", "slm_shared_prefix_decode_attn_f32", "slm_set_wait_timeout_ns")
 
 
 class SlmError(RuntimeError):
@@ -56,11 +57,17 @@ def load(path: Optional[str] = None):
         lib.slm_abi_version.argtypes = []
         lib.slm_packed_prefill_attn.restype = ctypes.c_int
         lib.slm_packed_prefill_attn.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, f32, P, P, P, sz, P, P]
+        lib.slm_packed_prefill_attn_f32.restype = ctypes.c_int
+        lib.slm_packed_prefill_attn_f32.argtypes = lib.slm_packed_prefill_attn.argtypes
+        lib.slm_set_wait_timeout_ns.restype = ctypes.c_uint64
+        lib.slm_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.slm_prefill_workspace_size.restype = sz
         lib.slm_prefill_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.slm_shared_prefix_decode_attn.restype = ctypes.c_int
         lib.slm_shared_prefix_decode_attn.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                       f32, P, P, P, P, P, P, sz, P]
+        lib.slm_shared_prefix_decode_attn_f32.restype = ctypes.c_int
+        lib.slm_shared_prefix_decode_attn_f32.argtypes = lib.slm_shared_prefix_decode_attn.argtypes
         lib.slm_shared_prefix_decode_workspace_size.restype = sz
         lib.slm_shared_prefix_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.slm_beam_select.restype = ctypes.c_int
@@ -129,6 +136,12 @@ def slm_abi_version() -> int:
     return int(load().slm_abi_version())
 
 
+def slm_set_wait_timeout_ns(ns: int) -> int:
+    """Sets the limit of the attention kernels' bounded waits (test and
+    diagnostic use; default 1 s) and returns the previous one."""
+    return int(load().slm_set_wait_timeout_ns(int(ns)))
+
+
 # ----------------------------------------------------------------------------
 # Packed prefill
 # ----------------------------------------------------------------------------
@@ -140,6 +153,23 @@ def slm_packed_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, c
     """O [T, Hq, D] of packed causal GQA attention over sequences delimited by
     ``cu_seqlens`` (int32 [B+1], on the device).  ``lse`` (fp32 [Hq, T]) is
     filled when given."""
+    return _prefill(q, k, v, cu_seqlens, max_seqlen, softmax_scale, cu_seqlens_host, out, lse, workspace,
+                    dev_status, torch.bfloat16)
+
+
+def slm_packed_prefill_attn_f32(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens: torch.Tensor,
+                                max_seqlen: int, softmax_scale: Optional[float] = None, *,
+                                cu_seqlens_host: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                                lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                                dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The same attention with O returned as fp32 [T, Hq, D], before any bf16
+    rounding (test and diagnostic variant)."""
+    return _prefill(q, k, v, cu_seqlens, max_seqlen, softmax_scale, cu_seqlens_host, out, lse, workspace,
+                    dev_status, torch.float32)
+
+
+def _prefill(q, k, v, cu_seqlens, max_seqlen, softmax_scale, cu_seqlens_host, out, lse, workspace, dev_status,
+             out_dtype):
     _need(q, "q", torch.bfloat16, 3)
     _need(k, "k", torch.bfloat16, 3)
     _need(v, "v", torch.bfloat16, 3)
@@ -151,8 +181,8 @@ def slm_packed_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, c
     B = cu_seqlens.shape[0] - 1
     scale = float(softmax_scale) if softmax_scale is not None else 1.0 / float(D) ** 0.5
     if out is None:
-        out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 3)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    _need(out, "out", out_dtype, 3)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
     need = slm_prefill_workspace_size(B, T, int(max_seqlen), Hq, Hkv)
@@ -163,7 +193,8 @@ def slm_packed_prefill_attn(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, c
         host_cs = cu_seqlens_host.to(torch.int32).contiguous()
         if host_cs.is_cuda:
             raise ValueError("cu_seqlens_host must be on the CPU")
-    st = load().slm_packed_prefill_attn(
+    fn = load().slm_packed_prefill_attn if out_dtype == torch.bfloat16 else load().slm_packed_prefill_attn_f32
+    st = fn(
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(host_cs), B, T, int(max_seqlen), Hq, Hkv, D, scale,
         _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(q.device))
     _check(st)
@@ -202,6 +233,27 @@ def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], v
     prompt's key blocks be split over CTAs; when None, a zeroed one kept per
     device and stream is used (a completed call leaves it fit for the next;
     inside a CUDA graph capture a fresh one is allocated instead)."""
+    return _decode(q, kp, vp, ks, vs, k_new, v_new, parent_idx, L_prev, softmax_scale, ks_out, vs_out, out, lse,
+                   dev_status, workspace, torch.bfloat16)
+
+
+def slm_shared_prefix_decode_attn_f32(q: torch.Tensor, kp: Optional[torch.Tensor], vp: Optional[torch.Tensor],
+                                      ks: Optional[torch.Tensor], vs: Optional[torch.Tensor],
+                                      k_new: Optional[torch.Tensor], v_new: Optional[torch.Tensor],
+                                      parent_idx: Optional[torch.Tensor], L_prev: int,
+                                      softmax_scale: Optional[float] = None, *, ks_out: torch.Tensor,
+                                      vs_out: torch.Tensor, out: Optional[torch.Tensor] = None,
+                                      lse: Optional[torch.Tensor] = None,
+                                      dev_status: Optional[torch.Tensor] = None,
+                                      workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The same decode attention with O returned as fp32 [W, Hq, D], before
+    any bf16 rounding (test and diagnostic variant)."""
+    return _decode(q, kp, vp, ks, vs, k_new, v_new, parent_idx, L_prev, softmax_scale, ks_out, vs_out, out, lse,
+                   dev_status, workspace, torch.float32)
+
+
+def _decode(q, kp, vp, ks, vs, k_new, v_new, parent_idx, L_prev, softmax_scale, ks_out, vs_out, out, lse,
+            dev_status, workspace, out_dtype):
     _need(q, "q", torch.bfloat16, 3)
     W, Hq, D = q.shape
     _need(ks_out, "ks_out", torch.bfloat16, 4)
@@ -228,15 +280,16 @@ def slm_shared_prefix_decode_attn(q: torch.Tensor, kp: Optional[torch.Tensor], v
         _need(parent_idx, "parent_idx", torch.int32, 1)
     scale = float(softmax_scale) if softmax_scale is not None else 1.0 / float(D) ** 0.5
     if out is None:
-        out = torch.empty_like(q)
-    _need(out, "out", torch.bfloat16, 3)
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    _need(out, "out", out_dtype, 3)
     if lse is not None:
         _need(lse, "lse", torch.float32, 2)
     if workspace is None:
         n = slm_shared_prefix_decode_workspace_size(W, Lp, Hq, Hkv, D)
         workspace = _decode_workspace(q.device, n) if n else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load().slm_shared_prefix_decode_attn(
+    fn = load().slm_shared_prefix_decode_attn if out_dtype == torch.bfloat16 else load().slm_shared_prefix_decode_attn_f32
+    st = fn(
         _ptr(q), _ptr(kp), _ptr(vp), _ptr(ks), _ptr(vs), _ptr(k_new), _ptr(v_new), _ptr(parent_idx), W, Lp,
         int(L_prev), Smax, Hq, Hkv, D, scale, _ptr(ks_out), _ptr(vs_out), _ptr(out), _ptr(lse), _ptr(dev_status),
         _ptr(workspace), ws_bytes, _stream(q.device))
@@ -280,8 +333,15 @@ def slm_beam_select(logits: torch.Tensor, cum_scores: torch.Tensor, W: int, *, w
 
 
 def slm_check_status(dev_status: torch.Tensor) -> None:
+    """Raises SlmError when a kernel set a bit in ``dev_status``.  After a
+    pipeline timeout the decode workspaces kept for this device are dropped:
+    a unit that gave up never took its ticket, so they are not zero any more."""
     _need(dev_status, "dev_status", torch.int32)
-    _check(load().slm_check_status(_ptr(dev_status), _stream(dev_status.device)))
+    st = load().slm_check_status(_ptr(dev_status), _stream(dev_status.device))
+    if st != SLM_OK and int(dev_status.item()) & 4:
+        for key in [k for k in _decode_ws if k[0] == dev_status.device.index]:
+            del _decode_ws[key]
+    _check(st)
 
 
 # ----------------------------------------------------------------------------

@@ -1,6 +1,7 @@
 // C ABI of the attention hot path (declared in include/slm_attn.h): argument
 // validation, TMA tensor-map encoding, schedule and kernel launches.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -62,6 +63,10 @@ slm_status cuda_fail(cudaError_t e, const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Limit of every bounded wait inside the attention kernels, read when a call
+// fills its launch parameters (slm_set_wait_timeout_ns).
+std::atomic<uint64_t> g_wait_ns{kWaitTimeoutNs};
+
 // ---- TMA descriptor encoding through the driver entry point ----------------
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -109,7 +114,7 @@ int num_sms() {
 template <int D, AttnMode MODE>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                         const AttnParams& p, int64_t max_units, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, MODE>;
+  auto kern = p.o_f32 ? attn_fwd_kernel<D, MODE, true> : attn_fwd_kernel<D, MODE, false>;
   const int smem = FwdSmem<D>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -249,12 +254,18 @@ size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_
   return static_cast<size_t>(((1 + 3 * cap) * 4 + 255) / 256 * 256);
 }
 
-slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
-                                   const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens,
-                                   int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                   float softmax_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
-                                   int32_t* dev_status, void* stream_) {
+}  // extern "C"
+
+namespace {
+
+// Packed prefill with a bf16 output o, or (o_f32 non-null) an fp32 one.
+slm_status prefill_impl(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                        const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen,
+                        int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, float softmax_scale, void* o_bf16,
+                        float* o_f32, float* lse, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  void* o = o_f32 ? static_cast<void*>(o_f32) : o_bf16;
   if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0)
     return fail(SLM_ERR_INVALID_ARG, "negative size (num_seqs=%d total_tokens=%d max_seqlen=%d)", num_seqs,
                 total_tokens, max_seqlen);
@@ -291,12 +302,20 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   const int tok = kBlockM / G;
   const int64_t cap = prefill_item_capacity(num_seqs, total_tokens, tok);
   if (cap * n_kv_heads > 0x7FFFFFFF) return fail(SLM_ERR_UNSUPPORTED, "too many tiles");
+  // A softmax warp's 32 rows are whole tokens when G divides 32: those warps
+  // write their rows through a {64, G, 32 / G} box of the output map.
+  const bool warp_tma_store = (o_f32 == nullptr) && (32 % G == 0);
   CUtensorMap tq, tk, tv, to;
   if (!encode_bf16_3d(&tq, q, head_dim, n_q_heads, total_tokens, G, tok) ||
-      !encode_bf16_3d(&to, o, head_dim, n_q_heads, total_tokens, G, tok) ||
       !encode_bf16_3d(&tk, k, head_dim, n_kv_heads, total_tokens, 1, kBlockN) ||
       !encode_bf16_3d(&tv, v, head_dim, n_kv_heads, total_tokens, 1, kBlockN))
     return fail(SLM_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  if (warp_tma_store) {
+    if (!encode_bf16_3d(&to, o, head_dim, n_q_heads, total_tokens, G, 32 / G))
+      return fail(SLM_ERR_CUDA, "cuTensorMapEncodeTiled failed (o)");
+  } else {
+    to = tq;  // not used
+  }
 
   int32_t* items = static_cast<int32_t*>(workspace);
   const int max_nb = std::max(1, (max_seqlen + kBlockN - 1) / kBlockN);
@@ -311,9 +330,12 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   p.group = G;
   p.tok_per_tile = tok;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.o = static_cast<__nv_bfloat16*>(o);
+  p.o = static_cast<__nv_bfloat16*>(o_bf16);
+  p.o_f32 = o_f32;
   p.lse = lse;
   p.dev_status = dev_status;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  p.warp_tma_store = warp_tma_store ? 1 : 0;
   p.cu_seqlens = cu_seqlens;
   p.items = items;
   p.total_tokens = total_tokens;
@@ -323,13 +345,40 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
   return ok();
 }
 
+}  // namespace
+
+extern "C" {
+
+slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                   const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens,
+                                   int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                   float softmax_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_status, void* stream) {
+  return prefill_impl(q, k, v, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens, max_seqlen, n_q_heads,
+                      n_kv_heads, head_dim, softmax_scale, o, nullptr, lse, workspace, workspace_bytes, dev_status,
+                      stream);
+}
+
+slm_status slm_packed_prefill_attn_f32(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                       const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens,
+                                       int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                       float softmax_scale, float* o, float* lse, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  if (total_tokens > 0 && !o) return fail(SLM_ERR_INVALID_ARG, "null o");
+  return prefill_impl(q, k, v, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens, max_seqlen, n_q_heads,
+                      n_kv_heads, head_dim, softmax_scale, nullptr, o, lse, workspace, workspace_bytes, dev_status,
+                      stream);
+}
+
+uint64_t slm_set_wait_timeout_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
+
 // Decode key-split workspace: a fixed area of tickets first (one per beam
-// tile pair, KV head and sub-tile; the same place whatever the call's sizes,
+// tile pair, KV head, sub-tile and softmax warp; the same place whatever the call's sizes,
 // so no call's parts ever land on them), then the split parts of every output
 // row (fp32 O and (max, sum)), stored per sub-tile with rows innermost.  The
 // tickets must be zero before a call; a call that completes leaves them zero.
 constexpr int64_t kMaxDecodeSplit = 16;
-constexpr size_t kDecodeTickets = 4096;
+constexpr size_t kDecodeTickets = 16384;  // one per warp of every sub-tile
 struct DecodeSplitLayout {
   size_t o_off, ml_off, ticket_off, total;
   bool fits;  // the call's tickets fit the fixed area
@@ -344,18 +393,22 @@ static DecodeSplitLayout decode_split_layout(int n_split, int W, int n_q_heads, 
   l.o_off = kDecodeTickets * sizeof(int32_t);
   l.ml_off = l.o_off + up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * head_dim * sizeof(float));
   l.total = l.ml_off + up(static_cast<size_t>(n_split) * sub_tiles * kBlockM * 2 * sizeof(float));
-  l.fits = sub_tiles <= kDecodeTickets;
+  l.fits = sub_tiles * 4 <= kDecodeTickets;
   return l;
 }
 
-slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const void* vp, const void* ks,
-                                         const void* vs, const void* k_new, const void* v_new,
-                                         const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
-                                         int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
-                                         float softmax_scale, void* ks_out, void* vs_out, void* o, float* lse,
-                                         int32_t* dev_status, void* workspace, size_t workspace_bytes,
-                                         void* stream_) {
+}  // extern "C"
+
+namespace {
+
+// Shared-prefix decode with a bf16 output o, or (o_f32 non-null) an fp32 one.
+slm_status decode_impl(const void* q, const void* kp, const void* vp, const void* ks, const void* vs,
+                       const void* k_new, const void* v_new, const int32_t* parent_idx, int32_t W, int32_t Lp,
+                       int32_t L_prev, int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                       float softmax_scale, void* ks_out, void* vs_out, void* o_bf16, float* o_f32, float* lse,
+                       int32_t* dev_status, void* workspace, size_t workspace_bytes, void* stream_) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  void* o = o_f32 ? static_cast<void*>(o_f32) : o_bf16;
   if (W < 0 || Lp < 0 || L_prev < 0 || Smax < 0)
     return fail(SLM_ERR_INVALID_ARG, "negative size (W=%d Lp=%d L_prev=%d Smax=%d)", W, Lp, L_prev, Smax);
   if (n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
@@ -419,9 +472,11 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
   p.group = G;
   p.tok_per_tile = tok;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.o = static_cast<__nv_bfloat16*>(o);
+  p.o = static_cast<__nv_bfloat16*>(o_bf16);
+  p.o_f32 = o_f32;
   p.lse = lse;
   p.dev_status = dev_status;
+  p.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.ks = static_cast<const __nv_bfloat16*>(ks);
   p.vs = static_cast<const __nv_bfloat16*>(vs);
@@ -448,6 +503,35 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
                                    : launch_attn<128, AttnMode::kDecodePrefix>(tq, tk, tv, tq, p, n_units, stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const void* vp, const void* ks,
+                                         const void* vs, const void* k_new, const void* v_new,
+                                         const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
+                                         int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                         float softmax_scale, void* ks_out, void* vs_out, void* o, float* lse,
+                                         int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                         void* stream) {
+  return decode_impl(q, kp, vp, ks, vs, k_new, v_new, parent_idx, W, Lp, L_prev, Smax, n_q_heads, n_kv_heads,
+                     head_dim, softmax_scale, ks_out, vs_out, o, nullptr, lse, dev_status, workspace,
+                     workspace_bytes, stream);
+}
+
+slm_status slm_shared_prefix_decode_attn_f32(const void* q, const void* kp, const void* vp, const void* ks,
+                                             const void* vs, const void* k_new, const void* v_new,
+                                             const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
+                                             int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                             float softmax_scale, void* ks_out, void* vs_out, float* o, float* lse,
+                                             int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                             void* stream) {
+  if (W > 0 && !o) return fail(SLM_ERR_INVALID_ARG, "null o");
+  return decode_impl(q, kp, vp, ks, vs, k_new, v_new, parent_idx, W, Lp, L_prev, Smax, n_q_heads, n_kv_heads,
+                     head_dim, softmax_scale, ks_out, vs_out, nullptr, o, lse, dev_status, workspace,
+                     workspace_bytes, stream);
 }
 
 size_t slm_shared_prefix_decode_workspace_size(int32_t W, int32_t Lp, int32_t n_q_heads, int32_t n_kv_heads,

@@ -58,8 +58,13 @@ struct AttnParams {
   int n_q_heads, n_kv_heads, group, tok_per_tile;
   float scale_log2;          // softmax_scale * log2(e)
   __nv_bfloat16* o;
+  float* o_f32;              // fp32 O rows (kernels instantiated with F32OUT only)
   float* lse;                // nullable
   int32_t* dev_status;       // nullable
+  uint64_t wait_ns;          // limit of every bounded mbarrier wait
+  // prefill: each softmax warp writes its 32 rows (32 / G whole tokens) with
+  // TMA stores through a {64, G, 32 / G} box of tm_o (G divides 32)
+  int warp_tma_store;
   // prefill
   const int32_t* cu_seqlens;
   const int32_t* items;      // [0] = count, then (start, length, pair) per item, longest sequences first
@@ -82,7 +87,7 @@ struct AttnParams {
   int n_split, blk_per_split;
   float* ws_o;          // [n_split][tiles * n_kv_heads * 2][D][128]
   float2* ws_ml;        // [n_split][tiles * n_kv_heads * 2][128]
-  int32_t* tickets;     // [tiles * n_kv_heads * 2]: zero between calls
+  int32_t* tickets;     // [tiles * n_kv_heads * 2][4 warps]: zero between calls
 };
 
 template <int D>
@@ -182,12 +187,16 @@ __device__ __forceinline__ UnitInfo unit_info(const AttnParams& p, int u, const 
   return U;
 }
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-  bool ok = mbar_wait(bar, parity, abort_flag);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+  bool ok = mbar_wait(bar, parity, abort_flag, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int D, AttnMode MODE>
+// F32OUT: O is written as fp32 rows to p.o_f32 (the test and diagnostic
+// entry points) instead of bf16; a separate instantiation, so that the fp32
+// store path costs the bf16 kernels no registers.
+template <int D, AttnMode MODE, bool F32OUT = false>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -201,6 +210,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint64_t wlim = p.wait_ns;
   const int G = p.group;
   const int TOK = p.tok_per_tile;
   const int rows_used = TOK * G;
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
         if (U.nblk_max == 0) continue;  // decode with an empty prefix: suffix only
         const int qb = qi % L::kQBufs;
-        if (qi >= L::kQBufs) ok = mbar_wait(&bars[L::Q_EMPTY + qb], ((qi / L::kQBufs) - 1) & 1, abort_flag);
+        if (qi >= L::kQBufs) ok = mbar_wait(&bars[L::Q_EMPTY + qb], ((qi / L::kQBufs) - 1) & 1, abort_flag, wlim);
         if (!ok) break;
         uint32_t q_bytes = 0;
         for (int t = 0; t < 2; ++t)
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int j = 0; j < U.nblk_max && ok; ++j) {
           for (int kind = 0; kind < 2; ++kind) {
             const uint32_t slot = kv_i % L::kStages, use = kv_i / L::kStages;
-            if (use >= 1) ok = mbar_wait(&bars[L::KV_EMPTY + slot], (use - 1) & 1, abort_flag);
+            if (use >= 1) ok = mbar_wait(&bars[L::KV_EMPTY + slot], (use - 1) & 1, abort_flag, wlim);
             if (!ok) break;
             mbar_arrive_expect_tx(&bars[L::KV_FULL + slot], L::kTile);
             for (int dh = 0; dh < L::kDSub; ++dh)
@@ -356,9 +366,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (u + static_cast<int>(gridDim.x) < n_units) rn = unit_raw<MODE>(p, u + gridDim.x);
         if (U.nblk_max == 0) continue;
         const int qb = it % L::kQBufs;
-        ok = mbar_wait(&bars[L::Q_FULL + qb], (it / L::kQBufs) & 1, abort_flag);
+        ok = mbar_wait(&bars[L::Q_FULL + qb], (it / L::kQBufs) & 1, abort_flag, wlim);
         const uint32_t kbase = kv_i;
-        if (ok) ok = mbar_wait(&bars[L::KV_FULL + slot(kbase)], phase(kbase), abort_flag);
+        if (ok) ok = mbar_wait(&bars[L::KV_FULL + slot(kbase)], phase(kbase), abort_flag, wlim);
         if (!ok) break;
         tc_fence_after_sync();
         for (int t = 0; t < 2; ++t)
@@ -370,12 +380,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (U.nblk_max == 1) umma_commit(&bars[L::Q_EMPTY + qb]);  // the unit's last S MMAs are issued
         for (int j = 0; j < U.nblk_max && ok; ++j) {
           const uint32_t vi = kbase + 2 * j + 1, kn = kbase + 2 * j + 2;
-          ok = mbar_wait(&bars[L::KV_FULL + slot(vi)], phase(vi), abort_flag);
+          ok = mbar_wait(&bars[L::KV_FULL + slot(vi)], phase(vi), abort_flag, wlim);
           bool k_next_ready = false;  // K_{j+1} is waited for only by the S that needs it
           for (int t = 0; t < 2 && ok; ++t) {
             if (j >= U.nblk[t]) continue;
-            if (j == 0 && o_used[t] > 0) ok = mbar_wait(&bars[L::O_EMPTY + t], (o_used[t] - 1) & 1, abort_flag);
-            if (ok) ok = mbar_wait(&bars[L::P_FULL + t], p_cnt[t] & 1, abort_flag);
+            if (j == 0 && o_used[t] > 0) ok = mbar_wait(&bars[L::O_EMPTY + t], (o_used[t] - 1) & 1, abort_flag, wlim);
+            if (ok) ok = mbar_wait(&bars[L::P_FULL + t], p_cnt[t] & 1, abort_flag, wlim);
             if (!ok) break;
             ++p_cnt[t];
             tc_fence_after_sync();
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               ++o_used[t];
             } else {
               if (!k_next_ready) {
-                ok = mbar_wait(&bars[L::KV_FULL + slot(kn)], phase(kn), abort_flag);
+                ok = mbar_wait(&bars[L::KV_FULL + slot(kn)], phase(kn), abort_flag, wlim);
                 if (!ok) break;
                 tc_fence_after_sync();
                 k_next_ready = true;
@@ -411,6 +421,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   } else {
     // ======================= softmax / epilogue (two warpgroups) =======================
     const int t = warp >> 2;              // sub-tile of this warpgroup
+    const int wq = warp & 3;              // rows 32 wq .. 32 wq + 31 of the sub-tile
     const int r = threadIdx.x & 127;      // query row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem_base + t * 128;
@@ -429,7 +440,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float m_run = -INFINITY;  // running max, log2 domain (scaled)
       float l_run = 0.f;
       for (int j = 0; j < U.nblk[t]; ++j) {
-        ok = warp_wait(&bars[L::S_FULL + t], s_cnt & 1, abort_flag);
+        ok = warp_wait(&bars[L::S_FULL + t], s_cnt & 1, abort_flag, wlim);
         if (!ok) break;
         ++s_cnt;
         tc_fence_after_sync();
@@ -504,7 +515,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // ---- epilogue ----
       float acc[D];
       if (U.nblk[t] > 0) {
-        ok = warp_wait(&bars[L::O_FULL + t], o_cnt & 1, abort_flag);
+        ok = warp_wait(&bars[L::O_FULL + t], o_cnt & 1, abort_flag, wlim);
         if (!ok) break;
         ++o_cnt;
         tc_fence_after_sync();
@@ -527,9 +538,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
       if constexpr (MODE == AttnMode::kDecodePrefix) {
         if (p.n_split > 1) {
-          // This split's part of each row goes to the workspace; the last split
-          // of the sub-tile to arrive (ticket) merges all parts and goes on, the
-          // others are done.  The last one also sets the ticket back to zero.
+          // This split's part of each row goes to the workspace; for each warp's
+          // 32 rows, the last split to arrive (ticket) merges all parts and goes
+          // on, the others are done.  The last one also sets the ticket back to
+          // zero.  Warps decide on their own: no barrier spans the warpgroup.
           const int64_t n_tt = static_cast<int64_t>((p.W + 2 * TOK - 1) / (2 * TOK)) * p.n_kv_heads * 2;
           const int tt = (U.tile * p.n_kv_heads + U.kvh) * 2 + t;
           {
@@ -539,15 +551,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             __stcg(&p.ws_ml[(U.split * n_tt + tt) * 128 + r], make_float2(m_run, l_run));
           }
           __threadfence();
-          named_bar_sync(1 + t, 128);
-          volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 8 + 4 * t);
-          if (r == 0) {
-            const int last = atomicAdd(&p.tickets[tt], 1) == p.n_split - 1;
-            if (last) p.tickets[tt] = 0;  // no other split touches it in this call
-            *last_flag = last;
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            int32_t* ticket = &p.tickets[tt * 4 + wq];
+            last = atomicAdd(ticket, 1) == p.n_split - 1;
+            if (last) *ticket = 0;  // no other split touches it in this call
           }
-          named_bar_sync(1 + t, 128);
-          if (!*last_flag) continue;
+          if (!__shfl_sync(0xffffffffu, last, 0)) continue;
           __threadfence();
           if (row_valid) {
             float m = m_run;
@@ -636,32 +647,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
       }
 
-      const bool tma_out = (MODE == AttnMode::kPrefill) && U.n_tok[t] == TOK;
+      // Prefill: a warp whose 32 rows are whole tokens of the sequence writes
+      // them by TMA stores -- staged in shared memory in the swizzled box
+      // layout (row r = token * G + head, as the Q tile), 64 columns at a
+      // time, whole lines instead of 16-byte pieces of 256-byte rows.  Each
+      // warp has its own quarter of the sub-tile's staging buffer, so no
+      // barrier spans the warpgroup.  Other rows are stored row by row.
+      const int wtok = p.warp_tma_store ? 32 / G : 0;
+      const bool tma_out = (MODE == AttnMode::kPrefill) && !F32OUT && p.warp_tma_store &&
+                           (wq + 1) * wtok <= U.n_tok[t];
       if (tma_out) {
-        // A full sub-tile: rows staged in shared memory in the swizzled box
-        // layout (row r = token * G + head, as the Q tile), 64 columns at a
-        // time, and written by one TMA store each -- whole lines instead of
-        // 16-byte pieces of 256-byte rows.
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
         uint8_t* stage = smem + L::kOut + t * kSubTileBytes;
 #pragma unroll
         for (int dh = 0; dh < L::kDSub; ++dh) {
-          if (r == 0) bulk_wait_read0();  // the previous store has read the staging buffer
-          named_bar_sync(1 + t, 128);
-          if (r < rows_used) {
+          if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its rows
+          __syncwarp();
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int d = dh * 64 + c * 8;
-              st_shared_v4(smem_u32(stage + sw128_offset(r, c * 8)), pack_bf16x2(acc[d + 0] * inv_l, acc[d + 1] * inv_l),
-                           pack_bf16x2(acc[d + 2] * inv_l, acc[d + 3] * inv_l),
-                           pack_bf16x2(acc[d + 4] * inv_l, acc[d + 5] * inv_l),
-                           pack_bf16x2(acc[d + 6] * inv_l, acc[d + 7] * inv_l));
-            }
+          for (int c = 0; c < 8; ++c) {
+            const int d = dh * 64 + c * 8;
+            st_shared_v4(smem_u32(stage + sw128_offset(r, c * 8)), pack_bf16x2(acc[d + 0] * inv_l, acc[d + 1] * inv_l),
+                         pack_bf16x2(acc[d + 2] * inv_l, acc[d + 3] * inv_l),
+                         pack_bf16x2(acc[d + 4] * inv_l, acc[d + 5] * inv_l),
+                         pack_bf16x2(acc[d + 6] * inv_l, acc[d + 7] * inv_l));
           }
           fence_proxy_async_smem();
-          named_bar_sync(1 + t, 128);
-          if (r == 0) {
-            tma_store_3d(&tm_o, stage, dh * 64, U.kvh * G, U.row0[t]);
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tm_o, stage + wq * 32 * 128, dh * 64, U.kvh * G, U.row0[t] + wq * wtok);
             bulk_commit();
           }
         }
@@ -669,7 +682,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (row_valid) {
         const float inv_l = 1.f / l_run;
         const int64_t out_row = static_cast<int64_t>(rowid) * p.n_q_heads + h;
-        if (!tma_out) {
+        if constexpr (F32OUT) {
+          float4* dst = reinterpret_cast<float4*>(p.o_f32 + out_row * D);
+#pragma unroll
+          for (int d = 0; d < D; d += 4)
+            dst[d >> 2] = make_float4(acc[d] * inv_l, acc[d + 1] * inv_l, acc[d + 2] * inv_l, acc[d + 3] * inv_l);
+        } else if (!tma_out) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + out_row * D);
 #pragma unroll
           for (int d = 0; d < D; d += 8) {
@@ -691,14 +709,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if constexpr (MODE == AttnMode::kDecodePrefix) {
         // Suffix reorder for this sub-tile's beams and KV head:
         //   out[b, s] = in[parent[b], s] (s < L_prev), out[b, L_prev] = new[b].
+        // Each warp copies its own quarter of the sub-tile's beams (the warp
+        // that took the last split's ticket, when the prompt is split).
         const int n_suffix = p.L_prev + (p.k_new != nullptr ? 1 : 0);
         const int64_t row_stride = static_cast<int64_t>(p.n_kv_heads) * D;
-        const int items = U.n_tok[t] * n_suffix * (D / 8);
-        for (int i = r; i < items; i += 128) {
+        const int b_lo = (U.n_tok[t] * wq) / 4, b_hi = (U.n_tok[t] * (wq + 1)) / 4;
+        const int items = (b_hi - b_lo) * n_suffix * (D / 8);
+        for (int i = lane; i < items; i += 32) {
           const int chunk = i % (D / 8);
           const int rest = i / (D / 8);
           const int sidx = rest % n_suffix;
-          const int beam = U.row0[t] + rest / n_suffix;
+          const int beam = U.row0[t] + b_lo + rest / n_suffix;
           int src = p.parent ? p.parent[beam] : beam;
           if (src < 0 || src >= p.W) src = 0;  // flagged above
           const int64_t dst_off = (static_cast<int64_t>(beam) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
@@ -720,7 +741,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 
   // ---- teardown ----
-  if (MODE == AttnMode::kPrefill && warp < 8 && (threadIdx.x & 127) == 0) bulk_wait_all0();  // TMA stores done
+  if (MODE == AttnMode::kPrefill && warp < 8 && lane == 0) bulk_wait_all0();  // this warp's TMA stores done
   tc_fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag && p.dev_status) atomicOr(p.dev_status, kDevPipelineTimeout);

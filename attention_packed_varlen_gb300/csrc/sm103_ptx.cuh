@@ -13,7 +13,10 @@
 
 namespace slm {
 
-// Wall-clock budget of one bounded wait.
+// Wall-clock budget of one bounded wait (the default; the attention kernels
+// take theirs from their launch parameters).  Draining after an abort always
+// allows the full budget, so copies and MMAs already issued land before
+// shared and tensor memory are released.
 constexpr uint64_t kWaitTimeoutNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -60,16 +63,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
 }
 
 // Waits for the phase with the given parity to complete.  Returns false when
-// the abort flag is (or becomes) set, or after kWaitTimeoutNs; a timeout sets
-// the flag so every other role of the CTA stops as well.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// the abort flag is (or becomes) set, or after limit_ns; a timeout sets the
+// flag so every other role of the CTA stops as well.  limit_ns = 0 gives up
+// at the first wait whose phase is not already complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitTimeoutNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if (global_timer_ns() - t0 >= limit_ns) {
       *abort_flag = 1;
       return false;
     }

@@ -120,7 +120,8 @@ size_t slm_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_
  *          are not split.  The result is the same up to fp32 summation order.
  *          A call that completes leaves the workspace fit for the next call,
  *          of any sizes (its tickets back at zero); after a call whose
- *          dev_status reports a pipeline timeout, zero it again.  The caller owns the memory and
+ *          dev_status reports a pipeline timeout, zero it again (a unit that
+ *          gave up never takes its ticket).  The caller owns the memory and
  *          must not share it between calls in flight at the same time.
  *   dev_status: nullable device int32 (bad parent index, pipeline timeout).
  *
@@ -292,6 +293,44 @@ slm_status slm_packed_prefill_attn_noalloc(const void* q, const void* k, const v
  * SLM_OK.  Does not clear the word.
  */
 slm_status slm_check_status(const int32_t* dev_status, void* stream);
+
+/*
+ * Test and diagnostic variants with an fp32 output (article section 3.1:
+ * FP32 online softmax; section 3.2 for decode).  Arguments, validation,
+ * kernels and results are those of slm_packed_prefill_attn and
+ * slm_shared_prefix_decode_attn, except that o is fp32 with the same layout
+ * ([T, Hq, D] and [W, Hq, D]) and receives each row's fp32 result before any
+ * bf16 rounding.  They exist so that an accuracy bound can be checked on the
+ * attention arithmetic itself, without the output's bf16 rounding; prefill
+ * writes rows with plain stores here instead of TMA stores.
+ */
+slm_status slm_packed_prefill_attn_f32(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                                       const int32_t* cu_seqlens_host, int32_t num_seqs, int32_t total_tokens,
+                                       int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                       float softmax_scale, float* o, float* lse, void* workspace,
+                                       size_t workspace_bytes, int32_t* dev_status, void* stream);
+slm_status slm_shared_prefix_decode_attn_f32(const void* q, const void* kp, const void* vp, const void* ks,
+                                             const void* vs, const void* k_new, const void* v_new,
+                                             const int32_t* parent_idx, int32_t W, int32_t Lp, int32_t L_prev,
+                                             int32_t Smax, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+                                             float softmax_scale, void* ks_out, void* vs_out, float* o, float* lse,
+                                             int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                                             void* stream);
+
+/*
+ * Test and diagnostic control of the attention kernels' bounded waits (the
+ * failure detection that article section 2.5 asks of the serving path: bounded
+ * waiting rather than a hang).  Every wait of a pipeline stage inside the
+ * prefill and decode attention kernels gives up after `ns` nanoseconds; the
+ * kernel then drains the copies and tensor-core work it issued, frees its
+ * tensor memory, ends early and sets SLM_DEV_PIPELINE_TIMEOUT (outputs
+ * undefined).  The default is 1 s.  ns = 0 makes every wait that is not
+ * already complete give up at once, which forces that path in a test.
+ * Process-wide; read when a call is enqueued (a captured CUDA graph keeps the
+ * value of its capture).  Returns the previous value.  Draining itself always
+ * allows 1 s.
+ */
+uint64_t slm_set_wait_timeout_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -1,9 +1,17 @@
 """Comparison helpers for the GPU-vs-oracle parity tests.
 
-Attention outputs: the GPU writes bf16 O from fp32 accumulators; the oracle
-is fp64.  Per element the error must stay within max(1e-2, one bf16 ulp of
-the oracle value) -- above |O| = 2 a bf16 ulp exceeds 1e-2, so no bf16 output
-could meet 1e-2 there -- and the mean absolute error within 1e-3.
+Attention outputs.  The gate is max-abs 1e-2 and mean-abs 1e-3 against the
+fp64 oracle.  It is applied as it stands to the fp32 output of the test
+variants of the kernels (``fp32_gate=True``): that is the attention
+arithmetic itself.  The product output is bf16.  The kernel's fp32 result is
+off by the bf16 rounding of the softmax weights P before P V (relative 2^-8
+each, the unit roundoff of an 8-bit significand: at most 2^-8 sum_j w_j |v_j|)
+plus fp32 summation error, e32 <= 2^-8 sum_j w_j |v_j| + 1e-4; rounding that
+result to bf16 adds at most half a bf16 ulp of it (0.0078 for |O| in [2, 4),
+0.0156 in [4, 8)).  The bf16 output is therefore held per element to
+max(1e-2, e32 + half an ulp of |ref| + e32) when the caller passes
+sum_j w_j |v_j| (``weighted_abs_v``, the oracle run on |V|), else to the same
+with e32 = 1e-3; the mean-abs bound stays 1e-3.
 
 Beam selection: given the GPU's own fp32 log-normalisers, the oracle's full
 sort must give the GPU's candidates bit for bit.  Against the oracle's own
@@ -23,18 +31,21 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(e - 7)
 
 
-def check_attention(got: torch.Tensor, ref: np.ndarray, what: str = "", weighted_abs_v=None):
-    """weighted_abs_v (optional, same shape as ref): sum_j w_j |v_j| per
-    output, for inputs whose softmax is so peaked that the bf16 rounding of
-    the weights P (relative 2^-9 each) dominates: the element bound then
-    becomes 2^-9 * sum_j w_j |v_j| + one bf16 ulp of the output."""
+def check_attention(got: torch.Tensor, ref: np.ndarray, what: str = "", weighted_abs_v=None,
+                    fp32_gate: bool = False):
+    """got: the GPU output (bf16, or fp32 with fp32_gate); ref: the oracle's
+    fp64 result; weighted_abs_v (optional, same shape as ref): sum_j w_j |v_j|
+    per output.  Returns (max abs error, mean abs error)."""
     g = got.float().cpu().numpy().astype(np.float64)
     assert g.shape == ref.shape, (g.shape, ref.shape)
     assert np.isfinite(g).all(), f"{what}: non-finite output"
     err = np.abs(g - ref)
-    tol = np.maximum(ATOL_MAX, bf16_ulp(ref))
-    if weighted_abs_v is not None:
-        tol = np.maximum(tol, 2.0 ** -9 * weighted_abs_v + bf16_ulp(ref))
+    if fp32_gate:
+        assert got.dtype == torch.float32, "the gate applies to the fp32 output"
+        tol = np.full_like(ref, ATOL_MAX)
+    else:
+        e32 = 2.0 ** -8 * weighted_abs_v + 1e-4 if weighted_abs_v is not None else np.full_like(ref, 1e-3)
+        tol = np.maximum(ATOL_MAX, e32 + 0.5 * bf16_ulp(np.abs(ref) + e32))
     bad = err > tol
     assert not bad.any(), (f"{what}: {bad.sum()} elements out of tolerance; worst err {err.max():.4g} "
                            f"at {np.unravel_index(err.argmax(), err.shape)} (ref {ref.flat[err.argmax()]:.4g})")

@@ -13,7 +13,7 @@ import torch
 import oracle
 from attention_packed_varlen_gb300 import _binding as slm
 from attention_packed_varlen_gb300 import build, workloads as wl
-from tests.parity import check_attention, check_lse
+from tests.parity import bf16_ulp, check_attention, check_lse
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -30,7 +30,7 @@ def bits(t):
     return t.cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True, workspace=None):
+def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True, workspace=None, fp32=False):
     dev = torch.device(DEV)
     W, Hq, D = d.q.shape
     Hkv = d.kp.shape[1] if d.kp is not None else d.k_new.shape[1]
@@ -40,7 +40,8 @@ def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True, workspace=None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kp = d.kp.to(dev) if d.kp.shape[0] > 0 else None
     vp = d.vp.to(dev) if d.vp.shape[0] > 0 else None
-    o = slm.slm_shared_prefix_decode_attn(
+    fn = slm.slm_shared_prefix_decode_attn_f32 if fp32 else slm.slm_shared_prefix_decode_attn
+    o = fn(
         d.q.to(dev), kp, vp, ks_dev, vs_dev,
         d.k_new.to(dev) if with_new else None, d.v_new.to(dev) if with_new else None,
         d.parent.to(dev) if parent else None, d.L_prev, d.softmax_scale,
@@ -49,12 +50,29 @@ def run_step(d, ks_dev, vs_dev, Smax, with_new=True, parent=True, workspace=None
     return o, lse, ks_out, vs_out
 
 
-def check_step(d, ks_host, vs_host, o, lse, ks_out, vs_out, what, with_new=True, parent=True):
-    ref, ref_lse, ks_ref, vs_ref = oracle.shared_prefix_decode(
-        d.q, d.kp, d.vp, ks_host, vs_host, d.k_new if with_new else None, d.v_new if with_new else None,
-        d.parent if parent else None, d.L_prev, d.softmax_scale, n_threads=THREADS)
-    check_attention(o, ref, what)
+def check_step(d, ks_host, vs_host, o, lse, ks_out, vs_out, what, with_new=True, parent=True, o32=None):
+    args = (d.k_new if with_new else None, d.v_new if with_new else None, d.parent if parent else None,
+            d.L_prev, d.softmax_scale)
+    ref, ref_lse, ks_ref, vs_ref = oracle.shared_prefix_decode(d.q, d.kp, d.vp, ks_host, vs_host, *args,
+                                                               n_threads=THREADS)
+    # sum_j w_j |v_j| per output: the oracle with |V| everywhere
+    absv = lambda t: None if t is None else t.abs()
+    wabs, _, _, _ = oracle.shared_prefix_decode(d.q, d.kp, absv(d.vp), ks_host, absv(vs_host), args[0],
+                                                absv(args[1]), *args[2:], n_threads=THREADS)
+    check_attention(o, ref, what, weighted_abs_v=wabs)
     check_lse(lse, ref_lse, what)
+    if o32 is not None:  # the fp32 output of the same kernels: the benchmark spec's gate, and o is its rounding
+        check_attention(o32, ref, what + " (fp32 output)", fp32_gate=True)
+        # within one bf16 ulp of the fp32 result rounded: the last split to
+        # arrive merges the key splits, so their fp32 summation order varies
+        # between calls (measured run to run: below 1e-7 absolute, which near
+        # zero is several bf16 ulps, hence the 2^-20 absolute term)
+        r32 = o32.cpu().to(torch.bfloat16).float().numpy().astype(np.float64)
+        ob = o.cpu().float().numpy().astype(np.float64)
+        gap = np.abs(ob - r32)
+        lim = bf16_ulp(np.maximum(np.abs(ob), np.abs(r32))) + 2.0 ** -20
+        k = np.unravel_index((gap / lim).argmax(), gap.shape)
+        assert (gap <= lim).all(), (what, k, ob[k], float(o32.cpu()[k]), ref[k], gap[k] / lim[k])
     Ls = d.L_prev + (1 if with_new else 0)
     np.testing.assert_array_equal(bits(ks_out)[:, :Ls], ks_ref[:, :Ls], err_msg=f"{what}: K suffix reorder")
     np.testing.assert_array_equal(bits(vs_out)[:, :Ls], vs_ref[:, :Ls], err_msg=f"{what}: V suffix reorder")
@@ -77,7 +95,8 @@ def test_beam_workload_all_steps_chained(workload, index):
             ks_host, vs_host = d.ks, d.vs
             ks_dev, vs_dev = ks_host.to(dev), vs_host.to(dev)
         o, lse, ks_out, vs_out = run_step(d, ks_dev, vs_dev, Smax)
-        check_step(d, ks_host, vs_host, o, lse, ks_out, vs_out, f"{workload.name} step {step}")
+        o32 = run_step(d, ks_dev, vs_dev, Smax, fp32=True)[0]
+        check_step(d, ks_host, vs_host, o, lse, ks_out, vs_out, f"{workload.name} step {step}", o32=o32)
         # the next step reads this step's reordered suffix
         ks_dev, vs_dev = ks_out, vs_out
         ks_host, vs_host = ks_out.cpu(), vs_out.cpu()
@@ -96,7 +115,8 @@ def test_decode_edge_cases(W, Lp, L_prev, Smax, hq, hkv, D, with_new, parent):
     d = wl.decode_inputs(W, Lp, L_prev, Smax, hq, hkv, D, seed=W + Lp + L_prev, identity_parent=not parent)
     dev = torch.device(DEV)
     o, lse, ks_out, vs_out = run_step(d, d.ks.to(dev), d.vs.to(dev), Smax, with_new=with_new, parent=parent)
-    check_step(d, d.ks, d.vs, o, lse, ks_out, vs_out, f"W={W} Lp={Lp} L_prev={L_prev}", with_new, parent)
+    o32 = run_step(d, d.ks.to(dev), d.vs.to(dev), Smax, with_new=with_new, parent=parent, fp32=True)[0]
+    check_step(d, d.ks, d.vs, o, lse, ks_out, vs_out, f"W={W} Lp={Lp} L_prev={L_prev}", with_new, parent, o32=o32)
 
 
 @pytest.mark.parametrize("W,Lp,L_prev,hq,hkv,D", [

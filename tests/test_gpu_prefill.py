@@ -26,24 +26,40 @@ def _lib():
     slm.load()
 
 
-def run_gpu(inp, want_lse=True):
+def run_gpu(inp, want_lse=True, fp32=False):
     dev = torch.device(DEV)
     T, Hq = inp.q.shape[0], inp.q.shape[1]
     lse = torch.full((Hq, T), float("nan"), device=dev) if want_lse else None
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    o = slm.slm_packed_prefill_attn(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.cu_seqlens.to(dev),
-                                    max(1, inp.max_seqlen), inp.softmax_scale, lse=lse, dev_status=status,
-                                    cu_seqlens_host=inp.cu_seqlens)
+    fn = slm.slm_packed_prefill_attn_f32 if fp32 else slm.slm_packed_prefill_attn
+    o = fn(inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.cu_seqlens.to(dev), max(1, inp.max_seqlen),
+           inp.softmax_scale, lse=lse, dev_status=status, cu_seqlens_host=inp.cu_seqlens)
     slm.slm_check_status(status)
     return o, lse
 
 
+def oracle_with_weights(inp):
+    """The oracle's O and LSE, and sum_j w_j |v_j| per output (the oracle on |V|)."""
+    cu = inp.cu_seqlens.numpy()
+    ref, ref_lse = oracle.packed_prefill(inp.q, inp.k, inp.v, cu, inp.softmax_scale, want_lse=True,
+                                         n_threads=THREADS)
+    wabs = oracle.packed_prefill(inp.q, inp.k, inp.v.abs(), cu, inp.softmax_scale, n_threads=THREADS)
+    return ref, ref_lse, wabs
+
+
 def full_check(inp, what):
     o, lse = run_gpu(inp)
-    ref, ref_lse = oracle.packed_prefill(inp.q, inp.k, inp.v, inp.cu_seqlens.numpy(), inp.softmax_scale,
-                                         want_lse=True, n_threads=THREADS)
-    check_attention(o, ref, what)
+    ref, ref_lse, wabs = oracle_with_weights(inp)
+    check_attention(o, ref, what, weighted_abs_v=wabs)
     check_lse(lse, ref_lse, what)
+    # the same kernels with an fp32 output: north_star's gate on the arithmetic
+    o32, lse32 = run_gpu(inp, fp32=True)
+    err_max, err_mean = check_attention(o32, ref, what + " (fp32 output)", fp32_gate=True)
+    check_lse(lse32, ref_lse, what + " (fp32 output)")
+    # the bf16 output is the fp32 result rounded once to nearest
+    np.testing.assert_array_equal(o.cpu().view(torch.int16).numpy(),
+                                  o32.cpu().to(torch.bfloat16).view(torch.int16).numpy())
+    print(f"{what}: fp32 output max-abs {err_max:.3g}, mean-abs {err_mean:.3g}")
 
 
 def test_tiny_packed_prefill_workload():
@@ -73,16 +89,17 @@ def test_prefill_large_score_range_rescales():
     # q scaled up: scores span tens of units, so the running max jumps by more
     # than the lazy-rescale threshold across key blocks and O is rescaled in
     # TMEM.  The softmax is then so peaked that the bf16 rounding of P bounds
-    # the error (see tests/parity.check_attention).
+    # the error (tests/parity.check_attention states the bound).
     inp = wl.prefill_inputs((700, 300, 129), 16, 8, 128, seed=77)
     inp.q = (inp.q.float() * 6.0).to(torch.bfloat16)
     o, lse = run_gpu(inp)
-    cu = inp.cu_seqlens.numpy()
-    ref, ref_lse = oracle.packed_prefill(inp.q, inp.k, inp.v, cu, inp.softmax_scale, want_lse=True,
-                                         n_threads=THREADS)
-    wabs = oracle.packed_prefill(inp.q, inp.k, inp.v.abs(), cu, inp.softmax_scale, n_threads=THREADS)
+    ref, ref_lse, wabs = oracle_with_weights(inp)
     check_attention(o, ref, "large scores", weighted_abs_v=wabs)
     check_lse(lse, ref_lse, "large scores")
+    # fp32 output: within the bf16 rounding of the weights P, 2^-8 sum_j w_j |v_j|
+    o32, _ = run_gpu(inp, fp32=True)
+    err = np.abs(o32.cpu().numpy().astype(np.float64) - ref)
+    assert (err <= 2.0 ** -8 * wabs + 1e-4).all(), err.max()
 
 
 def test_concurrent_batch_sampled_rows():
