@@ -163,7 +163,7 @@ class ClockSampler:
 # capture of `bench.py --ncu-case prefill` (one layer of the same batch), keyed
 # by the code it was taken on (the kernel, its PTX helpers and the host launch,
 # comments and blank space left out); any other code reports null.
-PREFILL_TRAFFIC = {"fad776abb630d9de": 1.221418e9 + 0.512403e9}
+PREFILL_TRAFFIC = {"214d389d2e30d546": 1.230600e9 + 0.513426e9}
 
 
 def prefill_code_key() -> str:
@@ -358,6 +358,93 @@ def measure_decode_loop(dev, bw, seed, stop_id, stream, peaks, flush, reps=20, w
             "hbm_frac_of_measured": nbytes / graph_s / 1e9 / peaks["hbm_gbs"]}
 
 
+def measure_prefill_configs(dev, stream, peaks, flush, reps=50, warmup=10):
+    """The tiny packed prefill and the one-layer Prefill-Only request: median
+    of `reps` replays of the call (schedule + attention) captured in a CUDA
+    graph, cold (L2 flushed before each replay) and hot (the same inputs
+    again, L2 warm); the graph keeps host launch time out of both."""
+    from attention_packed_varlen_gb300 import _binding as slm
+    out = {}
+    for w, seed in ((wl.TINY_PREFILL, wl.workload_seed(1)), (wl.PREFILL_ONLY_REQUEST, wl.workload_seed(2))):
+        lengths = wl.draw_lengths(w.n_seqs, w.len_lo, w.len_hi, seed) if w.lengths is None else np.asarray(w.lengths)
+        T = int(lengths.sum())
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+        q = device_randn((T, w.n_q_heads, w.head_dim), gen, dev)
+        k = device_randn((T, w.n_kv_heads, w.head_dim), gen, dev)
+        v = device_randn((T, w.n_kv_heads, w.head_dim), gen, dev)
+        cu = wl.cu_seqlens_from_lengths(lengths).to(dev)
+        o = torch.empty_like(q)
+        ws = torch.empty(slm.slm_prefill_workspace_size(len(lengths), T, int(lengths.max()), w.n_q_heads,
+                                                        w.n_kv_heads), dtype=torch.uint8, device=dev)
+        call = lambda: slm.slm_packed_prefill_attn(q, k, v, cu, int(lengths.max()), w.softmax_scale, out=o,
+                                                   workspace=ws)
+        call()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        fn = graph.replay
+        flops = prefill_flops(lengths, w.n_q_heads, w.head_dim)
+        nbytes = prefill_bytes(T, w.n_q_heads, w.n_kv_heads, w.head_dim)
+        t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+        res = {"tokens": T, "gflop": flops / 1e9, "mbytes": nbytes / 1e6,
+               "roofline_floor_us": max(t_tensor, t_hbm) * 1e6,
+               "bound": "hbm" if t_hbm > t_tensor else "tensor"}
+        for kind, fl in (("cold", flush), ("hot", None)):
+            t = timed_reps(fn, stream, reps, warmup, fl)
+            res[kind] = {"us": t * 1e6, "tflops": flops / t / 1e12,
+                         "frac_of_bf16_burst": flops / t / 1e12 / peaks["bf16_tflops"],
+                         "frac_of_roofline_floor": max(t_tensor, t_hbm) / t,
+                         "hbm_gbs": nbytes / t / 1e9}
+        out[w.name] = res
+    return out
+
+
+def measure_decode_batched(dev, stream, peaks, flush, reps=20, warmup=3, R=16):
+    """R requests' decode attention (the last step of each beam workload:
+    longest suffix) back to back in one CUDA graph: sustained GB/s of the
+    attention alone, L2 flushed before each replay."""
+    from attention_packed_varlen_gb300 import _binding as slm
+    out = {}
+    for bw in BEAM_WLS:
+        W, Hq, Hkv, D, S = bw.beams, bw.n_q_heads, bw.n_kv_heads, bw.head_dim, bw.max_suffix
+        L_prev = bw.steps - 1
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(rank_beam_seed(bw, 0) + 31)
+        reqs = []
+        for _ in range(R):
+            reqs.append(dict(
+                q=device_randn((W, Hq, D), gen, dev), kp=device_randn((bw.prefix_len, Hkv, D), gen, dev),
+                vp=device_randn((bw.prefix_len, Hkv, D), gen, dev), ks=device_randn((W, S, Hkv, D), gen, dev),
+                vs=device_randn((W, S, Hkv, D), gen, dev), kn=device_randn((W, Hkv, D), gen, dev),
+                vn=device_randn((W, Hkv, D), gen, dev),
+                parent=torch.randint(0, W, (W,), generator=gen, device=dev, dtype=torch.int32),
+                ks_out=torch.empty((W, S, Hkv, D), dtype=torch.bfloat16, device=dev),
+                vs_out=torch.empty((W, S, Hkv, D), dtype=torch.bfloat16, device=dev),
+                o=torch.empty((W, Hq, D), dtype=torch.bfloat16, device=dev)))
+        n = slm.slm_shared_prefix_decode_workspace_size(W, bw.prefix_len, Hq, Hkv, D)
+        ws = torch.zeros(max(n, 16), dtype=torch.uint8, device=dev)
+
+        def all_calls():
+            for r in reqs:
+                slm.slm_shared_prefix_decode_attn(r["q"], r["kp"], r["vp"], r["ks"], r["vs"], r["kn"], r["vn"],
+                                                  r["parent"], L_prev, bw.softmax_scale, ks_out=r["ks_out"],
+                                                  vs_out=r["vs_out"], out=r["o"], workspace=ws if n else None)
+        all_calls()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            all_calls()
+        t = timed_reps(g.replay, stream, reps, warmup, flush)
+        nbytes = R * decode_attn_bytes(W, bw.prefix_len, L_prev, Hq, Hkv, D)
+        out[bw.name] = {"requests": R, "us_per_call": t * 1e6 / R, "bytes_per_call": nbytes / R,
+                        "sustained_gbs": nbytes / t / 1e9, "hbm_frac_of_measured": nbytes / t / 1e9 / peaks["hbm_gbs"],
+                        "l2": "flushed before each graph replay"}
+    return out
+
+
 def measure_heads(dev, stream, peaks, flush, T, reps=20, warmup=3):
     """Fused SwiGLU + per-token E4M3 over the concurrent batch's token rows
     (intermediate 5632), and last-token label scores of its 240 sequences."""
@@ -411,6 +498,46 @@ def oracle_prefill_sample(budget_s: float = 15.0):
             f"({done_flops / 1e9:.1f} GFLOP of the layer's {prefill_flops(lengths, w.n_q_heads, w.head_dim) / 1e9:.0f}), "
             f"{elapsed:.1f} s")
     return tflops, cores, desc
+
+
+def oracle_timings(budget_s: float = 8.0):
+    """The oracle as it stands on the host cores, single-threaded and on all
+    cores: prefill on whole sequences of the concurrent batch (about
+    budget_s each), one decode step of the long-prompt wide beam (W = 400,
+    4 history rows), and one beam selection of the short-prompt beam (a full
+    sort of 100 x 151,936 candidates; the sort is single-threaded)."""
+    import oracle
+    w = PREFILL_WL
+    lengths = wl.draw_lengths(w.n_seqs, w.len_lo, w.len_hi, PREFILL_SEED)
+    cores = oracle.default_threads()
+    res = {"cores": cores, "cpu": cpu_model()}
+    for threads in (1, cores):
+        done, elapsed, n_seq = 0.0, 0.0, 0
+        for b, L in enumerate(lengths):
+            if elapsed >= budget_s:
+                break
+            inp = wl.prefill_inputs([int(L)], w.n_q_heads, w.n_kv_heads, w.head_dim, seed=PREFILL_SEED * 1000 + b)
+            t0 = time.perf_counter()
+            oracle.packed_prefill(inp.q, inp.k, inp.v, inp.cu_seqlens.numpy(), inp.softmax_scale, n_threads=threads)
+            elapsed += time.perf_counter() - t0
+            done += prefill_flops([int(L)], w.n_q_heads, w.head_dim)
+            n_seq += 1
+        res[f"prefill_{threads}_threads"] = {"tflops": done / elapsed / 1e12, "sequences": n_seq, "s": elapsed}
+    bw = wl.LONG_PROMPT_WIDE_BEAM
+    d = wl.decode_inputs(bw.beams, bw.prefix_len, bw.steps - 1, bw.max_suffix, bw.n_q_heads, bw.n_kv_heads,
+                         bw.head_dim, seed=wl.workload_seed(5, bw.steps - 1))
+    for threads in (1, cores):
+        t0 = time.perf_counter()
+        oracle.shared_prefix_decode(d.q, d.kp, d.vp, d.ks, d.vs, d.k_new, d.v_new, d.parent, d.L_prev,
+                                    d.softmax_scale, n_threads=threads)
+        res[f"decode_attention_{threads}_threads"] = {"us_per_step": (time.perf_counter() - t0) * 1e6,
+                                                       "workload": bw.name}
+    bs = wl.SHORT_PROMPT_BEAM
+    s = wl.select_inputs(bs.beams, bs.vocab, bs.beams, seed=wl.workload_seed(4, 1), step=1)
+    t0 = time.perf_counter()
+    oracle.beam_select(s.logits, s.cum, 2 * bs.beams)
+    res["beam_select_1_thread"] = {"us_per_step": (time.perf_counter() - t0) * 1e6, "workload": bs.name}
+    return res
 
 
 def cpu_model():
@@ -620,14 +747,19 @@ def run_gpu(args):
         d2h = ho.numel() * 2 * args.e2e_layers
         e2e = {"value": job_throughput(ps.flops * args.e2e_layers, world, e2e_s) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "layers": args.e2e_layers}
+               "layers": args.e2e_layers,
+               # the copies overlap the attention: the link, not the kernel, bounds this figure
+               "h2d_gbs": h2d / e2e_s / 1e9, "d2h_gbs": d2h / e2e_s / 1e9}
 
     # the fused fixed-depth loop (one CUDA graph) and the head kernels, timed
     # after the main step with their own events
     flush = L2Flush(dev)
     decode_loop = {}
     heads = None
+    prefill_cfgs = decode_batched = None
     if not args.no_extra_legs:
+        prefill_cfgs = measure_prefill_configs(dev, stream, peaks, flush)
+        decode_batched = measure_decode_batched(dev, stream, peaks, flush)
         for j, bs in enumerate(beams):
             bw = bs.w
             decode_loop[bw.name] = {
@@ -637,13 +769,18 @@ def run_gpu(args):
         heads = measure_heads(dev, stream, peaks, flush, ps.T)
 
     cpu = None
+    oracle_t = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tfl, cores, desc = oracle_prefill_sample(budget_s=args.ref_budget)
         cpu = {"value": tfl, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "cpu": cpu_model()}
+        if not args.no_extra_legs:
+            oracle_t = oracle_timings()
 
     # prefill: schedule + attention; decode step: attention + 3 selection kernels
     launches_per_step = n_pre * 2 + sum(n_dec) * 4
     peak_sust = peaks["bf16_tflops_sustained"]
+    peak_burst = peaks["bf16_tflops"]
+    clocks = clk.summary()
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -655,15 +792,25 @@ def run_gpu(args):
             "l2": "inputs larger than L2: 28 distinct 1.6 GB layer sets per step",
             "parallelism": f"replicas x{world}",
         },
-        "prefill_pct_of_bf16_peak": {"sustained": value / world / peak_sust, "burst": value / world / peaks["bf16_tflops"]},
+        "prefill_pct_of_bf16_peak": {"burst": value / world / peak_burst, "sustained": value / world / peak_sust,
+                                     "sm_mhz": clocks.get("sm_mhz")},
         "decode": decode,
+        "decode_batched_graph": decode_batched,
+        "prefill_configs": prefill_cfgs,
         "decode_loop_graph": decode_loop,
         "heads": heads,
+        # the prefill runs at the maximum SM clock through the step (see
+        # clocks), so the burst peak is its denominator; the sustained one,
+        # measured at a lower clock under the power cap, is given beside it
         "roofline": {"kernel": "slm_packed_prefill_attn (schedule + tcgen05 attention)", "bound": "tensor",
-                     "achieved": achieved, "peak": peak_sust, "unit": "TFLOP/s", "frac": achieved / peak_sust,
-                     "peak_kind": f"bf16 sustained, {peaks['source']}",
-                     "hbm_achieved_gbs": ps.bytes / avg_launch_s / 1e9, "traffic": args.traffic if args.traffic is not None else prefill_traffic()},
-        "clocks": clk.summary(),
+                     "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s", "frac": achieved / peak_burst,
+                     "peak_kind": f"bf16 burst, {peaks['source']}",
+                     "frac_of_sustained": achieved / peak_sust, "sm_mhz": clocks.get("sm_mhz"),
+                     "hbm_achieved_gbs": ps.bytes / avg_launch_s / 1e9,
+                     "hbm_frac": ps.bytes / avg_launch_s / 1e9 / peaks["hbm_gbs"],
+                     "traffic": args.traffic if args.traffic is not None else prefill_traffic()},
+        "clocks": clocks,
+        "oracle_timings": oracle_t,
         "gpu_launches": launches_per_step * args.steps,
         "e2e": e2e,
         "cpu_baseline": cpu,
