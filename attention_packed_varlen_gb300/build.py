@@ -2,6 +2,11 @@
 
 Translation units compile in parallel, then link into one shared library next
 to this file.  The C ABI it exports is declared in ``include/slm_attn.h``.
+
+``build(debug=True)`` builds ``libslm_attn_debug.so`` instead: the same
+sources with ``-DSLM_DEBUG_BOUNDS`` (kernels check the indices they compute
+against their buffers and report a failed check in the device status word,
+never trapping) and ``-DSLM_NVTX`` (each entry point is an NVTX range).
 """
 from __future__ import annotations
 
@@ -17,6 +22,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libslm_attn.so")
+DEBUG_BUILD = os.path.join(PKG, "_build_debug")
+DEBUG_LIB = os.path.join(PKG, "libslm_attn_debug.so")
+DEBUG_FLAGS = ["-DSLM_DEBUG_BOUNDS", "-DSLM_NVTX"]
 
 SOURCES = ["api.cu", "beam_select.cu", "heads.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -37,22 +45,23 @@ def _deps() -> list:
     return out
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and not ptxas_info and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    lib_path, build_dir = (DEBUG_LIB, DEBUG_BUILD) if debug else (LIB, BUILD)
+    if not force and not ptxas_info and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (DEBUG_FLAGS if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,13 +72,13 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -16,6 +16,21 @@
 #include "slm_attn.h"
 #include "slm_internal.h"
 
+// Builds with -DSLM_NVTX mark every entry point as an NVTX range (host side)
+// for timeline tools; other builds have no NVTX dependency at all.
+#ifdef SLM_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace {
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+}  // namespace
+#define SLM_RANGE(name) NvtxRange slm_nvtx_range_(name)
+#else
+#define SLM_RANGE(name) ((void)0)
+#endif
+
 namespace slm {
 
 // Defined in beam_select.cu
@@ -145,7 +160,7 @@ constexpr int kBuckets = 4096;
 // round-robin, so the items of one sequence run at the same time on
 // different SMs and share its K/V through L2, and the short ones come last.
 __global__ void __launch_bounds__(kSchedThreads)
-    prefill_schedule_kernel(const int32_t* cu, int B, int T, int tok2, int max_nb, int32_t* items,
+    prefill_schedule_kernel(const int32_t* cu, int B, int T, int tok2, int max_nb, int32_t* items, int64_t cap,
                             int32_t* dev_status) {
   __shared__ int cnt[kBuckets];
   __shared__ int warp_tot[kSchedThreads / 32];
@@ -220,6 +235,7 @@ __global__ void __launch_bounds__(kSchedThreads)
     const int n_items = (len + tok2 - 1) / tok2;
     const int pos = atomicAdd(&cnt[(len + kBlockN - 1) / kBlockN], n_items);
     for (int k = 0; k < n_items; ++k) {
+      if (!in_bounds(pos + k < cap, dev_status)) break;
       items[1 + 3 * (pos + k)] = s0;
       items[2 + 3 * (pos + k)] = len;
       items[3 + 3 * (pos + k)] = n_items - 1 - k;
@@ -320,7 +336,7 @@ slm_status prefill_impl(const void* q, const void* k, const void* v, const int32
   int32_t* items = static_cast<int32_t*>(workspace);
   const int max_nb = std::max(1, (max_seqlen + kBlockN - 1) / kBlockN);
   prefill_schedule_kernel<<<1, kSchedThreads, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, 2 * tok, max_nb,
-                                                           items, dev_status);
+                                                           items, cap, dev_status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "prefill schedule launch");
 
@@ -338,6 +354,7 @@ slm_status prefill_impl(const void* q, const void* k, const void* v, const int32
   p.warp_tma_store = warp_tma_store ? 1 : 0;
   p.cu_seqlens = cu_seqlens;
   p.items = items;
+  p.items_cap = static_cast<int>(cap);
   p.total_tokens = total_tokens;
   e = (head_dim == 64) ? launch_attn<64, AttnMode::kPrefill>(tq, tk, tv, to, p, cap * n_kv_heads, stream)
                        : launch_attn<128, AttnMode::kPrefill>(tq, tk, tv, to, p, cap * n_kv_heads, stream);
@@ -354,6 +371,7 @@ slm_status slm_packed_prefill_attn(const void* q, const void* k, const void* v, 
                                    int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                    float softmax_scale, void* o, float* lse, void* workspace, size_t workspace_bytes,
                                    int32_t* dev_status, void* stream) {
+  SLM_RANGE("slm_packed_prefill_attn");
   return prefill_impl(q, k, v, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens, max_seqlen, n_q_heads,
                       n_kv_heads, head_dim, softmax_scale, o, nullptr, lse, workspace, workspace_bytes, dev_status,
                       stream);
@@ -364,6 +382,7 @@ slm_status slm_packed_prefill_attn_f32(const void* q, const void* k, const void*
                                        int32_t max_seqlen, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                        float softmax_scale, float* o, float* lse, void* workspace,
                                        size_t workspace_bytes, int32_t* dev_status, void* stream) {
+  SLM_RANGE("slm_packed_prefill_attn_f32");
   if (total_tokens > 0 && !o) return fail(SLM_ERR_INVALID_ARG, "null o");
   return prefill_impl(q, k, v, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens, max_seqlen, n_q_heads,
                       n_kv_heads, head_dim, softmax_scale, nullptr, o, lse, workspace, workspace_bytes, dev_status,
@@ -496,6 +515,8 @@ slm_status decode_impl(const void* q, const void* kp, const void* vp, const void
     p.ws_o = reinterpret_cast<float*>(ws + lay.o_off);
     p.ws_ml = reinterpret_cast<float2*>(ws + lay.ml_off);
     p.tickets = reinterpret_cast<int32_t*>(ws + lay.ticket_off);
+    p.ws_o_elems = static_cast<int64_t>((lay.ml_off - lay.o_off) / sizeof(float));
+    p.tickets_cap = static_cast<int>(kDecodeTickets);
   }
   // decode writes O row by row (the suffix merge ends in registers); the
   // output map argument is unused
@@ -516,6 +537,7 @@ slm_status slm_shared_prefix_decode_attn(const void* q, const void* kp, const vo
                                          float softmax_scale, void* ks_out, void* vs_out, void* o, float* lse,
                                          int32_t* dev_status, void* workspace, size_t workspace_bytes,
                                          void* stream) {
+  SLM_RANGE("slm_shared_prefix_decode_attn");
   return decode_impl(q, kp, vp, ks, vs, k_new, v_new, parent_idx, W, Lp, L_prev, Smax, n_q_heads, n_kv_heads,
                      head_dim, softmax_scale, ks_out, vs_out, o, nullptr, lse, dev_status, workspace,
                      workspace_bytes, stream);
@@ -528,6 +550,7 @@ slm_status slm_shared_prefix_decode_attn_f32(const void* q, const void* kp, cons
                                              float softmax_scale, void* ks_out, void* vs_out, float* o, float* lse,
                                              int32_t* dev_status, void* workspace, size_t workspace_bytes,
                                              void* stream) {
+  SLM_RANGE("slm_shared_prefix_decode_attn_f32");
   if (W > 0 && !o) return fail(SLM_ERR_INVALID_ARG, "null o");
   return decode_impl(q, kp, vp, ks, vs, k_new, v_new, parent_idx, W, Lp, L_prev, Smax, n_q_heads, n_kv_heads,
                      head_dim, softmax_scale, ks_out, vs_out, nullptr, o, lse, dev_status, workspace,
@@ -554,6 +577,7 @@ slm_status slm_beam_select(const void* logits, const float* cum_scores, int32_t 
                            int32_t* out_token, int32_t* out_parent, float* out_score, int32_t* out_cand_token,
                            int32_t* out_cand_parent, float* out_cand_score, float* out_lse, void* workspace,
                            size_t workspace_bytes, void* stream_) {
+  SLM_RANGE("slm_beam_select");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (W_in <= 0 || V <= 0 || W <= 0)
     return fail(SLM_ERR_INVALID_ARG, "sizes must be positive (W_in=%d V=%d W=%d)", W_in, V, W);
@@ -574,6 +598,7 @@ slm_status slm_beam_select(const void* logits, const float* cum_scores, int32_t 
 }
 
 slm_status slm_swiglu_quant_e4m3(const void* gate_up, int32_t T, int32_t I, void* q, float* scale, void* stream_) {
+  SLM_RANGE("slm_swiglu_quant_e4m3");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (T < 0 || I <= 0) return fail(SLM_ERR_INVALID_ARG, "need T >= 0 and I > 0 (T=%d I=%d)", T, I);
   if (I % 8 != 0) return fail(SLM_ERR_UNSUPPORTED, "I=%d must be a multiple of 8", I);
@@ -589,6 +614,7 @@ slm_status slm_swiglu_quant_e4m3(const void* gate_up, int32_t T, int32_t I, void
 slm_status slm_label_scores(const void* hidden, const int32_t* cu_seqlens, int32_t num_seqs, int32_t total_tokens,
                             int32_t d_model, const void* w_label, int32_t n_labels, float* logits, float* probs,
                             int32_t* dev_status, void* stream_) {
+  SLM_RANGE("slm_label_scores");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (num_seqs < 0 || total_tokens < 0 || d_model <= 0)
     return fail(SLM_ERR_INVALID_ARG, "bad sizes (num_seqs=%d total_tokens=%d d_model=%d)", num_seqs, total_tokens,
@@ -608,6 +634,7 @@ slm_status slm_beam_split_finished(const int32_t* cand_token, const int32_t* can
                                    int32_t W, int32_t stop_id, int32_t* out_token, int32_t* out_parent,
                                    float* out_score, int32_t* fin_token, int32_t* fin_parent, float* fin_score,
                                    int32_t* fin_count, void* stream_) {
+  SLM_RANGE("slm_beam_split_finished");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (W < 1 || W > 1024) return fail(SLM_ERR_INVALID_ARG, "W=%d outside [1, 1024]", W);
   if (!cand_token || !cand_parent || !cand_score || !out_token || !out_parent || !out_score || !fin_token ||
@@ -622,6 +649,7 @@ slm_status slm_beam_split_finished(const int32_t* cand_token, const int32_t* can
 slm_status slm_beam_reorder_history(const int32_t* hist_in, const int32_t* parent_idx, const int32_t* token,
                                     int32_t W, int32_t W_in, int32_t t, int32_t max_len, int32_t* hist_out,
                                     int32_t* dev_status, void* stream_) {
+  SLM_RANGE("slm_beam_reorder_history");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if (W < 1 || W_in < 1 || t < 0 || max_len < 1 || t >= max_len)
     return fail(SLM_ERR_INVALID_ARG, "bad sizes (W=%d W_in=%d t=%d max_len=%d)", W, W_in, t, max_len);
@@ -640,8 +668,9 @@ slm_status slm_check_status(const int32_t* dev_status, void* stream_) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return cuda_fail(e, "reading dev_status");
   if (h != 0)
-    return fail(SLM_ERR_DEVICE_CHECK, "device status 0x%x:%s%s%s", h, (h & kDevBadSeqlens) ? " bad-cu_seqlens" : "",
-                (h & kDevBadParent) ? " bad-parent-index" : "", (h & kDevPipelineTimeout) ? " pipeline-timeout" : "");
+    return fail(SLM_ERR_DEVICE_CHECK, "device status 0x%x:%s%s%s%s", h, (h & kDevBadSeqlens) ? " bad-cu_seqlens" : "",
+                (h & kDevBadParent) ? " bad-parent-index" : "", (h & kDevPipelineTimeout) ? " pipeline-timeout" : "",
+                (h & kDevBounds) ? " index-out-of-bounds" : "");
   return ok();
 }
 
@@ -696,6 +725,7 @@ extern "C" slm_status slm_packed_prefill_attn_noalloc(const void* q, const void*
                                                        int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
                                                        float softmax_scale, void* o, float* lse, int32_t* dev_status,
                                                        void* stream) {
+  SLM_RANGE("slm_packed_prefill_attn_noalloc");
   if (num_seqs < 0 || total_tokens < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0)
     return slm_packed_prefill_attn(q, k, v, cu_seqlens, cu_seqlens_host, num_seqs, total_tokens, max_seqlen,
                                    n_q_heads, n_kv_heads, head_dim, softmax_scale, o, lse, nullptr, 0, dev_status,

@@ -68,6 +68,7 @@ struct AttnParams {
   // prefill
   const int32_t* cu_seqlens;
   const int32_t* items;      // [0] = count, then (start, length, pair) per item, longest sequences first
+  int items_cap;             // items the workspace holds
   int total_tokens;
   // decode
   const __nv_bfloat16* q;    // read by the suffix merge
@@ -88,6 +89,8 @@ struct AttnParams {
   float* ws_o;          // [n_split][tiles * n_kv_heads * 2][D][128]
   float2* ws_ml;        // [n_split][tiles * n_kv_heads * 2][128]
   int32_t* tickets;     // [tiles * n_kv_heads * 2][4 warps]: zero between calls
+  int64_t ws_o_elems;   // floats in ws_o (bounds checks of debug builds)
+  int tickets_cap;      // ints in tickets
 };
 
 template <int D>
@@ -126,7 +129,10 @@ struct UnitInfo {
 
 template <AttnMode MODE>
 __device__ __forceinline__ int num_units(const AttnParams& p) {
-  if constexpr (MODE == AttnMode::kPrefill) return p.items[0] * p.n_kv_heads;
+  if constexpr (MODE == AttnMode::kPrefill) {
+    const int n = p.items[0];
+    return (in_bounds(n >= 0 && n <= p.items_cap, p.dev_status) ? n : 0) * p.n_kv_heads;
+  }
   else return ((p.W + 2 * p.tok_per_tile - 1) / (2 * p.tok_per_tile)) * p.n_kv_heads * p.n_split;
 }
 
@@ -169,6 +175,12 @@ __device__ __forceinline__ UnitInfo unit_info(const AttnParams& p, int u, const 
     }
     U.tile = item;
     U.split = 0;
+    // a work item must lie inside its sequence and the sequence inside the batch
+    if (!in_bounds(s0 >= 0 && len >= 1 && s0 + len <= p.total_tokens && pair >= 0 && 2 * pair * TOK < len,
+                   p.dev_status)) {
+#pragma unroll
+      for (int t = 0; t < 2; ++t) U.n_tok[t] = U.nblk[t] = 0;
+    }
   } else {
     U.split = item % p.n_split;
     U.tile = item / p.n_split;
@@ -544,6 +556,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           // zero.  Warps decide on their own: no barrier spans the warpgroup.
           const int64_t n_tt = static_cast<int64_t>((p.W + 2 * TOK - 1) / (2 * TOK)) * p.n_kv_heads * 2;
           const int tt = (U.tile * p.n_kv_heads + U.kvh) * 2 + t;
+          if (!in_bounds((U.split * n_tt + tt + 1) * D * 128 <= p.ws_o_elems && tt * 4 + wq < p.tickets_cap,
+                         p.dev_status))
+            continue;
           {
             float* dst = p.ws_o + (U.split * n_tt + tt) * D * 128 + r;
 #pragma unroll
@@ -655,7 +670,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // barrier spans the warpgroup.  Other rows are stored row by row.
       const int wtok = p.warp_tma_store ? 32 / G : 0;
       const bool tma_out = (MODE == AttnMode::kPrefill) && !F32OUT && p.warp_tma_store &&
-                           (wq + 1) * wtok <= U.n_tok[t];
+                           (wq + 1) * wtok <= U.n_tok[t] &&
+                           in_bounds(U.row0[t] + (wq + 1) * wtok <= p.total_tokens, p.dev_status);
       if (tma_out) {
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
         uint8_t* stage = smem + L::kOut + t * kSubTileBytes;
@@ -679,7 +695,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      if (row_valid) {
+      const int rows_total = (MODE == AttnMode::kPrefill) ? p.total_tokens : p.W;
+      if (row_valid && in_bounds(rowid >= 0 && rowid < rows_total && h < p.n_q_heads, p.dev_status)) {
         const float inv_l = 1.f / l_run;
         const int64_t out_row = static_cast<int64_t>(rowid) * p.n_q_heads + h;
         if constexpr (F32OUT) {

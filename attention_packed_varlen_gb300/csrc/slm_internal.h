@@ -9,5 +9,23 @@ namespace slm {
 constexpr int32_t kDevBadSeqlens = 1;        // sequence boundary not non-decreasing / not ending at T
 constexpr int32_t kDevBadParent = 2;         // parent index outside [0, W)
 constexpr int32_t kDevPipelineTimeout = 4;   // a bounded wait inside a kernel ran out
+constexpr int32_t kDevBounds = 8;            // debug-bounds builds: an index outside its buffer
+
+#if defined(__CUDACC__)
+// Builds with -DSLM_DEBUG_BOUNDS check the indices the kernels compute
+// against the buffers they address: a failed check ORs kDevBounds into the
+// status word and the caller skips the access (it never traps).  Other builds
+// compile the checks away.
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t* status) {
+#ifdef SLM_DEBUG_BOUNDS
+  if (!ok && status) atomicOr(status, kDevBounds);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
+#endif
 
 }  // namespace slm

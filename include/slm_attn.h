@@ -49,6 +49,8 @@ typedef enum {
 #define SLM_DEV_BAD_SEQLENS 1        /* cu_seqlens not non-decreasing from 0 to total_tokens */
 #define SLM_DEV_BAD_PARENT 2         /* a parent index outside [0, W) */
 #define SLM_DEV_PIPELINE_TIMEOUT 4   /* an in-kernel bounded wait ran out (kernel ended early) */
+#define SLM_DEV_BOUNDS 8             /* debug-bounds builds only (-DSLM_DEBUG_BOUNDS): an index a
+                                        kernel computed lay outside its buffer; the access was skipped */
 
 /* Thread-local description of the last failure on this thread ("" if none). */
 const char* slm_last_error(void);
