@@ -130,7 +130,7 @@ template <int D, AttnMode MODE>
 cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                         const AttnParams& p, int64_t max_units, cudaStream_t stream) {
   auto kern = p.o_f32 ? attn_fwd_kernel<D, MODE, true> : attn_fwd_kernel<D, MODE, false>;
-  const int smem = FwdSmem<D>::kAlloc;
+  const int smem = FwdSmem<D, MODE>::kAlloc;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), max_units)));

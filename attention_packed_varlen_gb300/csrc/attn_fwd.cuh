@@ -93,20 +93,29 @@ struct AttnParams {
   int tickets_cap;      // ints in tickets
 };
 
-template <int D>
+// Decode (D = 64): each softmax warp stages its beams' suffix rows (the
+// parents' history rows and the new rows, K and V, of its KV head) in its
+// own 8 KB, loaded with cp.async as the unit starts, so the suffix merge in
+// the epilogue reads shared memory instead of waiting on dependent loads.
+constexpr int kHistWarpBytes = 8192;
+
+template <int D, AttnMode MODE = AttnMode::kPrefill>
 struct FwdSmem {
   static constexpr int kDSub = D / 64;
   static constexpr int kTile = kDSub * kSubTileBytes;  // 128 rows x D bf16
   // D = 128: one Q buffer, released as soon as the unit's last S MMA is done,
   // so the K/V ring can hold 2 blocks and the next unit's first blocks
-  // arrive while the current unit ends.  D = 64: two Q buffers, 4 blocks.
-  // Both: 32 KB to stage O for TMA stores.
+  // arrive while the current unit ends.  D = 64: two Q buffers, 4 blocks
+  // (prefill) or 2 blocks and the suffix staging (decode).  Both: 32 KB to
+  // stage O for TMA stores.
+  static constexpr bool kHistStage = (MODE == AttnMode::kDecodePrefix) && (D == 64);
   static constexpr int kQBufs = (D == 128) ? 1 : 2;
-  static constexpr int kStages = (D == 128) ? 4 : 8;   // K/V ring
+  static constexpr int kStages = (D == 128) ? 4 : (kHistStage ? 4 : 8);  // K/V ring
   static constexpr int kQ = 0;                         // [kQBufs buffers][2 sub-tiles]
   static constexpr int kKV = kQ + 2 * kQBufs * kTile;
   static constexpr int kOut = kKV + kStages * kTile;   // [2 sub-tiles] 128 rows x 64 bf16: O staging for TMA stores
-  static constexpr int kBar = kOut + 2 * kSubTileBytes;
+  static constexpr int kHist = kOut + 2 * kSubTileBytes;  // [8 softmax warps] suffix rows (decode, D = 64)
+  static constexpr int kBar = kHist + (kHistStage ? 8 * kHistWarpBytes : 0);
   // barrier slots
   static constexpr int Q_FULL = 0, Q_EMPTY = 2, KV_FULL = 4, KV_EMPTY = KV_FULL + kStages,
                        S_FULL = KV_EMPTY + kStages, P_FULL = S_FULL + 2, O_FULL = P_FULL + 2,
@@ -213,7 +222,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const AttnParams p) {
-  using L = FwdSmem<D>;
+  using L = FwdSmem<D, MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
@@ -449,6 +458,52 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (U.n_tok[t] == 0) continue;
       const bool row_valid = (r < rows_used) && (t_loc < U.n_tok[t]);
       const int qpos = U.q0[t] + t_loc;
+      // Decode: this warp's beams' suffix rows, staged for the epilogue while
+      // the prompt's blocks run (rows hb_first .. of the sub-tile; layout
+      // [beam][suffix row][K, V][D]).
+      bool hist_staged = false;
+      int hb_first = 0;
+      const uint8_t* hist_w = nullptr;
+      if constexpr (L::kHistStage) {
+        const int n_suffix = p.L_prev + (p.k_new != nullptr ? 1 : 0);
+        hb_first = (32 * wq) / G;
+        const int nb = min((32 * wq + 31) / G, U.n_tok[t] - 1) - hb_first + 1;
+        hist_w = smem + L::kHist + (t * 4 + wq) * kHistWarpBytes;
+        if (n_suffix > 0 && nb > 0 && nb <= 8 && nb * n_suffix * 2 * D * 2 <= kHistWarpBytes) {
+          hist_staged = true;
+          cp_async_wait_all();  // the last unit's copies into this region have landed
+          int par = 0;          // parent of beam hb_first + lane
+          if (lane < nb) {
+            const int beam = U.row0[t] + hb_first + lane;
+            par = p.parent ? __ldg(p.parent + beam) : beam;
+            if (par < 0 || par >= p.W) par = 0;  // flagged by the epilogue
+          }
+          int pars[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) pars[k] = __shfl_sync(0xffffffffu, par, k);
+          const int64_t row_stride = static_cast<int64_t>(p.n_kv_heads) * D;
+          const int n_chunks = nb * n_suffix * 2 * (D / 8);
+          for (int i = lane; i < n_chunks; i += 32) {
+            const int c = i % (D / 8);
+            const int rest = i / (D / 8);
+            const int kind = rest & 1;
+            const int sidx = (rest >> 1) % n_suffix;
+            const int bb = (rest >> 1) / n_suffix;
+            int sp = pars[0];
+#pragma unroll
+            for (int k = 1; k < 8; ++k)
+              if (bb == k) sp = pars[k];
+            const __nv_bfloat16* src;
+            if (sidx < p.L_prev)
+              src = (kind ? p.vs : p.ks) + (static_cast<int64_t>(sp) * p.Smax + sidx) * row_stride + U.kvh * D + c * 8;
+            else
+              src = (kind ? p.v_new : p.k_new) + static_cast<int64_t>(U.row0[t] + hb_first + bb) * row_stride +
+                    U.kvh * D + c * 8;
+            cp_async_16(const_cast<uint8_t*>(hist_w) + i * 16, src);
+          }
+          cp_async_commit();
+        }
+      }
       float m_run = -INFINITY;  // running max, log2 domain (scaled)
       float l_run = 0.f;
       for (int j = 0; j < U.nblk[t]; ++j) {
@@ -597,6 +652,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // Suffix keys of this beam on CUDA cores: its parent's history rows
         // then its own new row, merged into the same online-softmax state.
+        if (hist_staged) {
+          cp_async_wait_all();
+          __syncwarp();  // every lane's staged rows are visible to the warp
+        }
         if (row_valid) {
           int src = rowid;
           if (p.parent) {
@@ -621,7 +680,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int sidx = 0; sidx < n_suffix; ++sidx) {
             const __nv_bfloat16* krow;
             const __nv_bfloat16* vrow;
-            if (sidx < p.L_prev) {
+            if (hist_staged) {
+              krow = reinterpret_cast<const __nv_bfloat16*>(hist_w) + ((t_loc - hb_first) * n_suffix + sidx) * 2 * D;
+              vrow = krow + D;
+            } else if (sidx < p.L_prev) {
               krow = p.ks + (static_cast<int64_t>(src) * p.Smax + sidx) * row_stride + U.kvh * D;
               vrow = p.vs + (static_cast<int64_t>(src) * p.Smax + sidx) * row_stride + U.kvh * D;
             } else {
@@ -631,7 +693,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             float dot = 0.f;
 #pragma unroll
             for (int d = 0; d < D; d += 8) {
-              const uint4 kv = __ldg(reinterpret_cast<const uint4*>(krow + d));
+              const uint4 kv = hist_staged ? ld_shared_v4(krow + d) : __ldg(reinterpret_cast<const uint4*>(krow + d));
               const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -648,7 +710,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             l_run = l_run * alpha + pw;
 #pragma unroll
             for (int d = 0; d < D; d += 8) {
-              const uint4 vv = __ldg(reinterpret_cast<const uint4*>(vrow + d));
+              const uint4 vv = hist_staged ? ld_shared_v4(vrow + d) : __ldg(reinterpret_cast<const uint4*>(vrow + d));
               const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&vv);
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
@@ -759,6 +821,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   // ---- teardown ----
   if (MODE == AttnMode::kPrefill && warp < 8 && lane == 0) bulk_wait_all0();  // this warp's TMA stores done
+  if (FwdSmem<D, MODE>::kHistStage && warp < 8) cp_async_wait_all();       // staged suffix rows have landed
   tc_fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort_flag && p.dev_status) atomicOr(p.dev_status, kDevPipelineTimeout);
