@@ -788,32 +788,49 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if constexpr (MODE == AttnMode::kDecodePrefix) {
         // Suffix reorder for this sub-tile's beams and KV head:
         //   out[b, s] = in[parent[b], s] (s < L_prev), out[b, L_prev] = new[b].
-        // Each warp copies its own quarter of the sub-tile's beams (the warp
-        // that took the last split's ticket, when the prompt is split).
+        // Each warp copies the beams whose first row it holds (the warp that
+        // took the last split's ticket, when the prompt is split), from its
+        // staged rows when it has them.
         const int n_suffix = p.L_prev + (p.k_new != nullptr ? 1 : 0);
         const int64_t row_stride = static_cast<int64_t>(p.n_kv_heads) * D;
-        const int b_lo = (U.n_tok[t] * wq) / 4, b_hi = (U.n_tok[t] * (wq + 1)) / 4;
-        const int items = (b_hi - b_lo) * n_suffix * (D / 8);
-        for (int i = lane; i < items; i += 32) {
-          const int chunk = i % (D / 8);
-          const int rest = i / (D / 8);
-          const int sidx = rest % n_suffix;
-          const int beam = U.row0[t] + b_lo + rest / n_suffix;
-          int src = p.parent ? p.parent[beam] : beam;
-          if (src < 0 || src >= p.W) src = 0;  // flagged above
-          const int64_t dst_off = (static_cast<int64_t>(beam) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
-          uint4 kv, vv;
-          if (sidx < p.L_prev) {
-            const int64_t src_off = (static_cast<int64_t>(src) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
-            kv = __ldg(reinterpret_cast<const uint4*>(p.ks + src_off));
-            vv = __ldg(reinterpret_cast<const uint4*>(p.vs + src_off));
-          } else {
-            const int64_t src_off = static_cast<int64_t>(beam) * row_stride + U.kvh * D + chunk * 8;
-            kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src_off));
-            vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src_off));
+        const int b_lo = min((32 * wq + G - 1) / G, U.n_tok[t]);
+        const int b_hi = min((32 * (wq + 1) + G - 1) / G, U.n_tok[t]);
+        if (hist_staged) {
+          const int items = (b_hi - b_lo) * n_suffix * 2 * (D / 8);
+          for (int i = lane; i < items; i += 32) {
+            const int chunk = i % (D / 8);
+            const int rest = i / (D / 8);
+            const int kind = rest & 1;
+            const int sidx = (rest >> 1) % n_suffix;
+            const int bb = b_lo + (rest >> 1) / n_suffix;
+            const uint4 v = ld_shared_v4(hist_w + ((((bb - hb_first) * n_suffix + sidx) * 2 + kind) * (D / 8) + chunk) * 16);
+            const int64_t dst_off =
+                (static_cast<int64_t>(U.row0[t] + bb) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
+            *reinterpret_cast<uint4*>((kind ? p.vs_out : p.ks_out) + dst_off) = v;
           }
-          *reinterpret_cast<uint4*>(p.ks_out + dst_off) = kv;
-          *reinterpret_cast<uint4*>(p.vs_out + dst_off) = vv;
+        } else {
+          const int items = (b_hi - b_lo) * n_suffix * (D / 8);
+          for (int i = lane; i < items; i += 32) {
+            const int chunk = i % (D / 8);
+            const int rest = i / (D / 8);
+            const int sidx = rest % n_suffix;
+            const int beam = U.row0[t] + b_lo + rest / n_suffix;
+            int src = p.parent ? p.parent[beam] : beam;
+            if (src < 0 || src >= p.W) src = 0;  // flagged above
+            const int64_t dst_off = (static_cast<int64_t>(beam) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
+            uint4 kv, vv;
+            if (sidx < p.L_prev) {
+              const int64_t src_off = (static_cast<int64_t>(src) * p.Smax + sidx) * row_stride + U.kvh * D + chunk * 8;
+              kv = __ldg(reinterpret_cast<const uint4*>(p.ks + src_off));
+              vv = __ldg(reinterpret_cast<const uint4*>(p.vs + src_off));
+            } else {
+              const int64_t src_off = static_cast<int64_t>(beam) * row_stride + U.kvh * D + chunk * 8;
+              kv = __ldg(reinterpret_cast<const uint4*>(p.k_new + src_off));
+              vv = __ldg(reinterpret_cast<const uint4*>(p.v_new + src_off));
+            }
+            *reinterpret_cast<uint4*>(p.ks_out + dst_off) = kv;
+            *reinterpret_cast<uint4*>(p.vs_out + dst_off) = vv;
+          }
         }
       }
     }
