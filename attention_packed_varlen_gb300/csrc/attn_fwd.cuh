@@ -656,6 +656,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           cp_async_wait_all();
           __syncwarp();  // every lane's staged rows are visible to the warp
         }
+        // A CTA with a single unit still holds its Q tile (buffer 0, never
+        // reloaded): the q rows come from there instead of global memory.
+        const bool q_in_smem = n_units <= static_cast<int>(gridDim.x) && U.nblk_max > 0;
+        if (q_in_smem) {
+          ok = warp_wait(&bars[L::Q_FULL], 0, abort_flag, wlim);  // completed long ago: orders the TMA's writes
+          if (!ok) break;
+        }
         if (row_valid) {
           int src = rowid;
           if (p.parent) {
@@ -669,7 +676,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           const __nv_bfloat16* qrow = p.q + (static_cast<int64_t>(rowid) * p.n_q_heads + h) * D;
 #pragma unroll
           for (int d = 0; d < D; d += 8) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4*>(qrow + d));
+            const uint4 v = q_in_smem ? ld_shared_v4(q_tile(0, t) + (d / 64) * kSubTileBytes + sw128_offset(r, d % 64))
+                                      : __ldg(reinterpret_cast<const uint4*>(qrow + d));
             q2[d / 2 + 0] = v.x;
             q2[d / 2 + 1] = v.y;
             q2[d / 2 + 2] = v.z;
