@@ -182,3 +182,37 @@ def test_graph_replay_equals_eager_and_takes_new_inputs(stop_id):
             else:
                 assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                                    b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
+
+
+def test_graph_replays_repeat_the_same_beams():
+    # Many replays of the wide-beam loop: every selection, history and
+    # reordered suffix must repeat bit for bit (the logits are inputs, so
+    # nothing upstream of a selection varies), and the attention output may
+    # differ only by the key-split merge's fp32 summation order.  A race in
+    # any kernel's pipeline would show up here as a replay that differs.
+    bw = wl.LONG_PROMPT_WIDE_BEAM
+    d = wl.decode_loop_inputs(bw, 21)
+    static = to_dev(d)
+    loop = make_loop(bw, None)
+    loop.record(*static)
+    torch.cuda.synchronize()
+    loop.capture(*static)
+    loop.replay()
+    torch.cuda.synchronize()
+    first = snapshot(loop)
+    for _ in range(30):
+        loop.replay()
+    torch.cuda.synchronize()
+    slm.slm_check_status(loop.status)
+    last = snapshot(loop)
+    for key in ("hist", "ks", "vs"):
+        for a, b in zip(first[key], last[key]):
+            assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
+    for a, b in zip(first["sel"], last["sel"]):
+        for k in a:
+            assert torch.equal(a[k], b[k]), ("sel", k)
+    for a, b in zip(first["o"], last["o"]):
+        gap = (a.float() - b.float()).abs()
+        lim = torch.maximum(a.float().abs(), b.float().abs()) * 2.0 ** -7 + 2.0 ** -20
+        assert bool((gap <= lim).all()), float(gap.max())

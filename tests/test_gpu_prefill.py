@@ -138,7 +138,10 @@ def test_prefill_bad_boundary_sets_device_status():
 
 
 def test_prefill_repeatable():
+    # the prefill has no order-dependent reduction: repeated calls agree bit
+    # for bit (a race in the pipeline would show up as a call that differs)
     inp = wl.prefill_workload_inputs(wl.PREFILL_ONLY_REQUEST, seed=5)
     a, _ = run_gpu(inp, want_lse=False)
-    b, _ = run_gpu(inp, want_lse=False)
-    assert torch.equal(a, b)
+    for _ in range(10):
+        b, _ = run_gpu(inp, want_lse=False)
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
