@@ -16,7 +16,7 @@
 // a group whose maximum scores >= L, and is itself >= L.  Only those groups
 // are read again, and only their logits scoring >= L are ranked.
 //
-// Three kernels, the logits read once from HBM plus a few hundred small groups:
+// Two kernels, the logits read once from HBM plus a few hundred small groups:
 //
 // 1. stream (persistent, one CTA per SM): a producer warp streams 16 KB tiles
 //    into a 12-stage shared-memory ring with 1-D bulk copies (cp.async.bulk)
@@ -24,13 +24,10 @@
 //    whole tiles: the maximum of each of the tile's 128 sub-chunks (packed
 //    bf16x2 max), then the tile's sum of exp(x - M_t) relative to its
 //    maximum (packed f32x2 FMA and ex2).  Per tile it writes (M_t, sum) and the 128 sub-chunk maxima.
-// 2. row statistics (a warp per beam, or a CTA per beam when the groups are
-//    sub-chunks; a programmatic dependent of the stream): lse_b from the
-//    beam's tile partials in a fixed order, each group's best score key, and
-//    a histogram of the keys' upper 16 bits with their maximum.
-// 3. select (one CTA per SM, a programmatic dependent of the row kernel):
-//    every CTA walks the histogram down to the bin holding the 2W-th largest
-//    group key -- its lower edge is L, at most that key -- lists the groups
+// 2. select (one CTA per SM, a programmatic dependent of the stream): every
+//    CTA derives lse_b of every beam from the tile partials (a thread per
+//    beam, its tiles in order) and every group's best score key into shared
+//    memory, radix-selects the 2W-th largest key as L, lists the groups
 //    scoring >= L in group order, and takes its share of them: it reads
 //    their sub-chunks scoring >= L back from the logits and appends the
 //    logits scoring >= L to a small list.  The last CTA to finish ranks that
@@ -38,6 +35,13 @@
 //    writes the 2W results.  If the list would overflow (huge score ties)
 //    the last CTA ranks every logit scoring >= L exactly with a radix select
 //    instead.
+//
+// Shapes whose group keys do not fit the select kernel's shared memory (more
+// than 16,384 groups, or rows of more than 64 tiles) run a row-statistics
+// kernel between the two (a warp per beam, or a CTA per beam when the groups
+// are sub-chunks): lse_b, the group keys and a histogram of their upper 16
+// bits in global memory; every select CTA then walks the histogram down to
+// the bin holding the 2W-th largest key and takes that bin's lower edge as L.
 //
 // Every wait on an mbarrier is bounded; a wait that runs out marks the call
 // failed and the outputs are filled with -1 ids and NaN scores.
@@ -63,7 +67,7 @@ constexpr int kStages = 12;                        // ring depth (192 KB)
 constexpr int kStreamThreads = 32 * (kCWarps + 1);
 constexpr int kQuarters = 4;                       // sub-chunks per lane and tile (2 chunks each)
 constexpr int kSubPerTile = kQuarters * 32;        // 128 sub-chunks of 64 logits per tile
-constexpr int kSelThreads = 1024;
+constexpr int kSelThreads = 1024;                  // select kernel threads (at most 1024: 32 warps)
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kRowThreads = 256;                   // row-statistics kernel: a warp per beam
 constexpr int kRowWarps = kRowThreads / 32;
@@ -288,6 +292,7 @@ struct Params {
   int W_in, V, K, W;       // K = 2W candidates kept globally
   int n_tpr, n_tiles;      // tiles per row, tiles in all
   bool vec_ok;             // rows 16-byte aligned: bulk copies and vector loads
+  bool fused;              // the select kernel derives the row statistics itself (no row kernel, no histogram)
   // workspace
   float2* partial;         // [n_tiles] (tile maximum M_t, sum of exp(x - M_t))
   uint16_t* submax;        // [n_tiles, kSubPerTile] sub-chunk maxima (bf16 bits)
@@ -471,7 +476,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     if (blockIdx.x == 0)
       for (int i = 0; i < kMiscWords; ++i) p.misc[i] = 0u;  // read by the select kernel after this grid ends
   }
-  {  // this CTA's slice of the group-key histogram (filled by the row kernel after this grid ends)
+  if (!p.fused) {  // this CTA's slice of the group-key histogram (filled by the row kernel after this grid ends)
     const int per = (kHistBins + gridDim.x - 1) / gridDim.x;
     const int end = min(kHistBins, (static_cast<int>(blockIdx.x) + 1) * per);
     for (int i = blockIdx.x * per + threadIdx.x; i < end; i += kStreamThreads) p.hist[i] = 0u;
@@ -492,33 +497,43 @@ struct Scratch {
   unsigned long long wu64[2][kSelWarps];
   int wint[kSelWarps];
   uint32_t wkey[kSelWarps];
-  int digit, above, in_bin, counter, flag, dstar;
+  int digit, above, in_bin, counter, flag, dstar, total;
   unsigned long long u64;
 };
 
+// Block-wide exclusive prefix sum and total.  The warps' totals are scanned
+// by warp 0 alone: every thread then reads two words of shared memory, where
+// a loop over the 32 warp totals in every thread costs ~1,000 cycles of the
+// shared-memory pipe.
 __device__ __forceinline__ int block_scan_excl(int v, int* total, Scratch& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int x = warp_inclusive_scan(v, lane);
   __syncthreads();
   if (lane == 31) sh.wint[w] = x;
   __syncthreads();
-  int base = 0, tot = 0;
-  for (int i = 0; i < kSelWarps; ++i) {
-    if (i < w) base += sh.wint[i];
-    tot += sh.wint[i];
+  if (w == 0) {
+    const int y = (lane < kSelWarps) ? sh.wint[lane] : 0;
+    const int inc = warp_inclusive_scan(y, lane);
+    sh.wint[lane] = inc - y;
+    if (lane == 31) sh.total = inc;
   }
-  *total = tot;
-  return base + x - v;
+  __syncthreads();
+  *total = sh.total;
+  return sh.wint[w] + x - v;
 }
 
+// Block-wide maximum (warp 0 reduces the warps' maxima).
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Scratch& sh) {
   v = warp_max_u32(v);
   __syncthreads();
   if ((threadIdx.x & 31) == 0) sh.wkey[threadIdx.x >> 5] = v;
   __syncthreads();
-  uint32_t r = 0;
-  for (int i = 0; i < kSelWarps; ++i) r = max(r, sh.wkey[i]);
-  return r;
+  if (threadIdx.x < 32) {
+    const uint32_t r = warp_max_u32((threadIdx.x < kSelWarps) ? sh.wkey[threadIdx.x] : 0u);
+    if (threadIdx.x == 0) sh.wkey[0] = r;
+  }
+  __syncthreads();
+  return sh.wkey[0];
 }
 
 // k-th largest (1-based, counting repeats) of the 64-bit keys all threads
@@ -541,12 +556,17 @@ __device__ unsigned long long block_kth(ForEach for_each, int k, Scratch& sh, un
     sh.wu64[1][w] = hi;
   }
   __syncthreads();
-  lo = ~0ull;
-  hi = 0ull;
-  for (int i = 0; i < kSelWarps; ++i) {
-    lo = min(lo, sh.wu64[0][i]);
-    hi = max(hi, sh.wu64[1][i]);
+  if (w == 0) {
+    const unsigned long long l = warp_min_u64((lane < kSelWarps) ? sh.wu64[0][lane] : ~0ull),
+                             h = warp_max_u64((lane < kSelWarps) ? sh.wu64[1][lane] : 0ull);
+    if (lane == 0) {
+      sh.wu64[0][0] = l;
+      sh.wu64[1][0] = h;
+    }
   }
+  __syncthreads();
+  lo = sh.wu64[0][0];
+  hi = sh.wu64[1][0];
   while (lo < hi) {
     const int sft = max(0, 64 - __clzll(hi - lo) - 8);
     for (int i = threadIdx.x; i < kSelWarps * 256; i += kSelThreads) (&whist[0][0])[i] = 0u;
@@ -620,7 +640,7 @@ __device__ __forceinline__ int next_pow2(int x) {
 }
 
 // ---------------------------------------------------------------------------
-// 2. row statistics (a warp per beam)
+// Row statistics for shapes beyond the fused path (a warp per beam)
 // ---------------------------------------------------------------------------
 // Score key fl32(cum + fl32(x - lse)), order-preserving.
 __device__ __forceinline__ uint32_t score_key_x(float x, float cum, float lse) {
@@ -694,11 +714,14 @@ __global__ void __launch_bounds__(kRowThreads) rowstat_kernel(const Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// 3. select
+// 2. select
 // ---------------------------------------------------------------------------
 constexpr int kBins = 4096;                      // final ranking bins
+constexpr int kKeyCap = 16384;                   // fused path: group keys held in shared memory
+constexpr int kFusedMaxTpr = 64;                 // fused path: tiles per row (a thread per beam sums them)
 constexpr int kUnitWords = 16384;                // ballot words: groups up to 524,288
 constexpr int kBinsPerThread = kBins / kSelThreads;
+constexpr int kCandPer = kCandCap / kSelThreads;  // candidates per thread in the final ranking
 static_assert(kBins % kSelThreads == 0, "whole bins per thread");
 static_assert(kUnitCap >= kCandCap, "the final ranking's order fits the group list");
 
@@ -706,22 +729,20 @@ static_assert(kUnitCap >= kCandCap, "the final ranking's order fits the group li
 struct SelSmem {
   float lse[kMaxRows];
   float cum[kMaxRows];
+  uint32_t keys[kKeyCap];     // fused path: every group's best score key
   int units[kUnitCap];        // groups scoring >= L (tiles, or sub-chunks t * 128 + s); the final ranking's lists
   unsigned bins[kBins];
   int fill[kBins];
   int rtok[2048], rpar[2048];  // the K results, written out together
   float rsc[2048];
   union {
-    struct {
-      unsigned long long hi[kCandCap];
-      uint32_t lo[kCandCap];
-    } c;                        // the last CTA's candidates, while they are ranked
-    ulonglong2 ent[kCandCap];   // the exact path's result, while it is sorted
+    ulonglong2 ent[kCandCap];   // the last CTA's candidates grouped by score bin; the exact path's result
     unsigned whist[kSelWarps][256];  // the exact path's radix histograms
     uint32_t words[kUnitWords];      // ballot words of the groups scoring >= L
   } u;
   Scratch sc;
 };
+static_assert(sizeof(SelSmem) <= 232448, "the select kernel's shared memory fits one CTA");
 
 // Result r of the global order into shared memory; error = true: -1 ids and NaN scores.
 __device__ __forceinline__ void stage_result(SelSmem& sm, int r, const ulonglong2& g, bool error = false) {
@@ -764,6 +785,106 @@ __device__ __forceinline__ uint4 load_run(const Params& p, int b, int col) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Fused path: every select CTA derives the row statistics itself from the
+// stream kernel's tile partials.  One coalesced pass loads every tile's
+// (M_t, sum) -- and, for sub-chunk groups, every sub-chunk maximum -- into
+// shared memory; a thread per beam then takes the beam's tiles in order for
+// lse_b (maximum, then the sum of the rescaled sums) and the group keys are
+// scored in place: the beam's tile maxima by that thread (tile groups), or
+// every sub-chunk maximum once all lse are known (sub-chunk groups).  The
+// arithmetic is the same in every CTA, so all CTAs hold the same lse and keys.
+__device__ uint32_t fused_row_stats(const Params& p, SelSmem& sm, bool tile_level, int n_groups) {
+  const int nt = p.n_tpr;
+  uint32_t mk = 0u;  // the largest key
+  // tile groups: M_t in the keys array (scored in place), sums in the union;
+  // sub-chunk groups (fewer than 2W <= 2048 tiles): both in the union
+  uint32_t* Mt = tile_level ? sm.keys : sm.u.words;
+  uint32_t* St = tile_level ? sm.u.words : sm.u.words + kUnitWords / 2;
+  for (int t = threadIdx.x; t < p.n_tiles; t += kSelThreads) {
+    const float2 q = __ldcg(p.partial + t);
+    Mt[t] = __float_as_uint(q.x);
+    St[t] = __float_as_uint(q.y);
+  }
+  if (!tile_level)
+    for (int g = threadIdx.x; g < n_groups; g += kSelThreads) sm.keys[g] = __ldcg(p.submax + g);
+  __syncthreads();
+  for (int b = threadIdx.x; b < p.W_in; b += kSelThreads) {
+    const uint32_t* m = Mt + b * nt;
+    const uint32_t* sb = St + b * nt;
+    float M = -INFINITY;
+#pragma unroll 4
+    for (int j = 0; j < nt; ++j)
+      if (__uint_as_float(sb[j]) > 0.f) M = fmaxf(M, __uint_as_float(m[j]));
+    float L = 0.f;
+#pragma unroll 4
+    for (int j = 0; j < nt; ++j) {
+      const float sj = __uint_as_float(sb[j]);
+      if (sj > 0.f) L += sj * ex2((__uint_as_float(m[j]) - M) * kLog2e);
+    }
+    const float lse = (L > 0.f) ? M + logf(L) : -INFINITY;
+    sm.lse[b] = lse;
+    if (blockIdx.x == 0 && p.out_lse) p.out_lse[b] = lse;
+    if (tile_level) {
+      const float cum = sm.cum[b];
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t key = score_key_x(__uint_as_float(m[j]), cum, lse);
+        sm.keys[b * nt + j] = key;
+        mk = max(mk, key);
+      }
+    }
+  }
+  if (!tile_level) {
+    __syncthreads();
+    for (int g = threadIdx.x; g < n_groups; g += kSelThreads) {
+      const int b = (g / kSubPerTile) / nt;
+      const uint32_t key = score_key_x(bf16_bits_to_f32(sm.keys[g]), sm.cum[b], sm.lse[b]);
+      sm.keys[g] = key;
+      mk = max(mk, key);
+    }
+  }
+  return block_max_u32(mk, sm.sc);  // its barriers also publish the keys
+}
+
+// Fused path: the lower edge of the bin of 2^16 keys that holds the K-th
+// largest group key, from a histogram of the keys' upper 16 bits counted down
+// from the largest key's (kBins bins in shared memory), or false when the
+// K-th key lies further down than kBins bins (then the caller selects
+// exactly).  `hist` is zero on entry.
+__device__ bool fused_threshold(const SelSmem& sm, int* hist, int n_groups, int K, uint32_t maxkey, Scratch& sh,
+                                uint32_t* Lk) {
+  const int tid = threadIdx.x;
+  const uint32_t top = maxkey >> 16;
+  if (tid == 0) sh.dstar = -1;
+  for (int g = tid; g < n_groups; g += kSelThreads) {
+    const uint32_t d = top - (sm.keys[g] >> 16);
+    if (d < static_cast<uint32_t>(kBins)) atomicAdd(hist + d, 1);
+  }
+  __syncthreads();
+  const int d0 = tid * kBinsPerThread;
+  int c[kBinsPerThread], local = 0;
+#pragma unroll
+  for (int i = 0; i < kBinsPerThread; ++i) {
+    c[i] = hist[d0 + i];
+    local += c[i];
+  }
+  int total;
+  int ex = block_scan_excl(local, &total, sh);
+  if (ex < K && ex + local >= K) {
+#pragma unroll
+    for (int i = 0; i < kBinsPerThread; ++i) {
+      if (ex < K && ex + c[i] >= K) sh.dstar = d0 + i;
+      ex += c[i];
+    }
+  }
+  __syncthreads();
+  const int dstar = sh.dstar;
+  __syncthreads();
+  if (dstar < 0) return false;
+  *Lk = (top - static_cast<uint32_t>(dstar)) << 16;
+  return true;
+}
+
+template <bool kFused>
 __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   SelSmem& sm = *reinterpret_cast<SelSmem*>(smem_raw);
@@ -777,18 +898,32 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
     sm.fill[i] = 0;
   }
   grid_dep_wait();
-  for (int b = tid; b < p.W_in; b += kSelThreads) sm.lse[b] = __ldcg(p.lse + b);
-  const uint32_t maxkey = __ldcg(p.misc + kMiscMaxKey);
-
   // the groups: tiles when there are at least K of them, else sub-chunks
   const bool tile_level = p.n_tiles >= K;
   const int n_groups = tile_level ? p.n_tiles : p.n_tiles * kSubPerTile;
+  uint32_t maxkey;
+  if constexpr (kFused) {
+    maxkey = fused_row_stats(p, sm, tile_level, n_groups);
+  } else {
+    for (int b = tid; b < p.W_in; b += kSelThreads) sm.lse[b] = __ldcg(p.lse + b);
+    maxkey = __ldcg(p.misc + kMiscMaxKey);
+  }
 
-  // L: the lower edge of the histogram bin that holds the K-th largest group
-  // key (bins walked down from the largest key's) -- at most that key, so at
-  // least K groups score >= L.  At most K groups: all of them.
+  // L: the lower edge of the bin of 2^16 keys that holds the K-th largest
+  // group key -- at most that key, so at least K groups score >= L.  Fused
+  // path: from a histogram of the keys in shared memory (or exactly that key,
+  // by radix select, when it lies far below the largest); otherwise: the
+  // global histogram walked down from the largest key's bin.  At most K
+  // groups: all of them.
   uint32_t Lk = 0u;
-  if (n_groups > K) {
+  if (kFused && n_groups > K) {
+    if (!fused_threshold(sm, sm.fill, n_groups, K, maxkey, sh, &Lk))
+      Lk = static_cast<uint32_t>(block_kth(
+          [&](auto f) {
+            for (int g = tid; g < n_groups; g += kSelThreads) f(static_cast<unsigned long long>(sm.keys[g]));
+          },
+          K, sh, sm.u.whist));
+  } else if (n_groups > K) {
     int carry = 0;
     if (tid == 0) sh.dstar = -1;
     for (int top = static_cast<int>(maxkey >> 16); top >= 0; top -= kSelThreads) {
@@ -819,7 +954,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int g = (w0 + i) * 32 + lane;
-        k8[i] = (w0 + i < w_hi && g < n_groups) ? __ldcg(p.gkeys + g) : 0u;
+        k8[i] = (w0 + i < w_hi && g < n_groups) ? (kFused ? sm.keys[g] : __ldcg(p.gkeys + g)) : 0u;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -829,14 +964,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
         cnt += __popc(bal);
       }
     }
-    if (lane == 0) sh.wint[warp] = cnt;
-    __syncthreads();
-    int pos = 0;
-    n_found = 0;
-    for (int i = 0; i < kSelWarps; ++i) {
-      if (i < warp) pos += sh.wint[i];
-      n_found += sh.wint[i];
-    }
+    // the warps' counts in warp order: lane 0 of each warp contributes its count
+    int pos = block_scan_excl(lane == 0 ? cnt : 0, &n_found, sh);
+    pos = __shfl_sync(kFull, pos, 0);
     for (int wd = w_lo; wd < w_hi; ++wd) {
       const unsigned bal = words[wd];
       const int at = pos + __popc(bal & ((1u << lane) - 1u));
@@ -946,15 +1076,19 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
       return min(static_cast<uint32_t>(static_cast<unsigned long long>(maxkey - min(skey, maxkey)) >> s2),
                  static_cast<uint32_t>(kBins - 1));
     };
-    for (int i = tid; i < n_cand; i += kSelThreads) {
-      const unsigned long long hi = __ldcg(&p.cand[i].x);
-      sm.u.c.hi[i] = hi;
-      sm.u.c.lo[i] = static_cast<uint32_t>(__ldcg(&p.cand[i].y));
-      atomicAdd(&sm.bins[bin_of(hi)], 1u);
+    // the candidates, up to kCandPer per thread, held in registers
+    unsigned long long ch[kCandPer], cl[kCandPer];
+#pragma unroll
+    for (int k = 0; k < kCandPer; ++k) {
+      const int i = tid + k * kSelThreads;
+      ch[k] = (i < n_cand) ? __ldcg(&p.cand[i].x) : 0ull;
+      cl[k] = (i < n_cand) ? __ldcg(&p.cand[i].y) : 0ull;
     }
+#pragma unroll
+    for (int k = 0; k < kCandPer; ++k)
+      if (tid + k * kSelThreads < n_cand) atomicAdd(&sm.bins[bin_of(ch[k])], 1u);
     __syncthreads();
     // bins -> first position of each bin (fill[] keeps the counts)
-    int* order = sm.units;  // entries grouped by bin
     {
       const int d0 = tid * kBinsPerThread;
       int cnt = 0;
@@ -971,25 +1105,22 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
       }
     }
     __syncthreads();
-    for (int i = tid; i < n_cand; i += kSelThreads) {
-      const uint32_t d = bin_of(sm.u.c.hi[i]);
-      order[static_cast<int>(atomicAdd(&sm.bins[d], 1u))] = i;  // bins[d] ends one past the bin
-    }
+    // the entries themselves, grouped by bin (bins in score order)
+#pragma unroll
+    for (int k = 0; k < kCandPer; ++k)
+      if (tid + k * kSelThreads < n_cand)
+        sm.u.ent[atomicAdd(&sm.bins[bin_of(ch[k])], 1u)] = make_ulonglong2(ch[k], cl[k]);  // bins[d]: one past the bin
     __syncthreads();
     // Each entry's rank: the entries of the bins above, plus those of its own
-    // bin that come before it.
-    for (int i = tid; i < n_cand; i += kSelThreads) {
-      const unsigned long long hi = sm.u.c.hi[i];
-      const uint32_t lo = sm.u.c.lo[i];
-      const uint32_t d = bin_of(hi);
+    // bin that come before it.  A warp's entries are neighbours in the grouped
+    // list, mostly of one bin, so its lanes read the same entries together.
+    for (int pos = tid; pos < n_cand; pos += kSelThreads) {
+      const ulonglong2 e = sm.u.ent[pos];
+      const uint32_t d = bin_of(e.x);
       const int g1 = static_cast<int>(sm.bins[d]), g0 = g1 - sm.fill[d];
       int rank = g0;
-      for (int j = g0; j < g1; ++j) {
-        const int o = order[j];
-        const unsigned long long hj = sm.u.c.hi[o];
-        rank += (hj > hi) | ((hj == hi) & (sm.u.c.lo[o] > lo));
-      }
-      if (rank < K) stage_result(sm, rank, make_ulonglong2(hi, lo));
+      for (int j = g0; j < g1; ++j) rank += entry_greater(sm.u.ent[j], e);
+      if (rank < K) stage_result(sm, rank, e);
     }
     write_results(p, sm);
     return;
@@ -1003,7 +1134,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
   auto for_each_entry = [&](auto f) {
     for (int u = 0; u < n_scan; ++u) {
       const int g = unit_over ? u : sm.units[u];
-      if (unit_over && __ldcg(p.gkeys + g) < Lk) continue;  // uniform: every thread reads the same key
+      if (unit_over && (kFused ? sm.keys[g] : __ldcg(p.gkeys + g)) < Lk) continue;  // uniform: the same key
       const int t = tile_level ? g : g / kSubPerTile;
       const int b = t / nt, c = t - b * nt;
       const float cum = sm.cum[b], lse = sm.lse[b];
@@ -1129,6 +1260,10 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   p.n_tpr = L.n_tpr;
   p.n_tiles = W_in * L.n_tpr;
   p.vec_ok = (V % 8 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+  {
+    const int64_t n_groups = p.n_tiles >= p.K ? int64_t(p.n_tiles) : int64_t(p.n_tiles) * sel::kSubPerTile;
+    p.fused = L.n_tpr <= sel::kFusedMaxTpr && n_groups <= sel::kKeyCap;
+  }
   p.partial = reinterpret_cast<float2*>(ws + L.off_partial);
   p.submax = reinterpret_cast<uint16_t*>(ws + L.off_submax);
   p.lse = reinterpret_cast<float*>(ws + L.off_lse);
@@ -1162,15 +1297,17 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(p.n_tiles < p.K ? W_in : (W_in + sel::kRowWarps - 1) / sel::kRowWarps);
-  cfg.blockDim = dim3(sel::kRowThreads);
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, sel::rowstat_kernel, p);
-  if (e != cudaSuccess) return e;
+  if (!p.fused) {
+    cfg.gridDim = dim3(p.n_tiles < p.K ? W_in : (W_in + sel::kRowWarps - 1) / sel::kRowWarps);
+    cfg.blockDim = dim3(sel::kRowThreads);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, sel::rowstat_kernel, p);
+    if (e != cudaSuccess) return e;
+  }
 
   const size_t smem_sel = sizeof(sel::SelSmem);
-  e = cudaFuncSetAttribute(sel::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_sel));
+  auto* select = p.fused ? sel::select_kernel<true> : sel::select_kernel<false>;
+  e = cudaFuncSetAttribute(select, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_sel));
   if (e != cudaSuccess) return e;
   // Narrow selections re-read a few hundred sub-chunks: 32 CTAs do it as fast
   // as a CTA per SM and reach the last-CTA ranking sooner (measured 22.5 ->
@@ -1178,7 +1315,7 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   cfg.gridDim = dim3(p.K <= 256 ? std::min(32, sm_count()) : sm_count());
   cfg.blockDim = dim3(sel::kSelThreads);
   cfg.dynamicSmemBytes = smem_sel;
-  return cudaLaunchKernelEx(&cfg, sel::select_kernel, p);
+  return cudaLaunchKernelEx(&cfg, select, p);
 }
 
 }  // namespace slm

@@ -58,6 +58,17 @@ def select_bytes(W_in, V) -> float:
     return float(W_in) * V * 2
 
 
+def select_launches(W_in, V, W) -> int:
+    """Kernels one slm_beam_select call launches: stream + select when the
+    group keys fit the select kernel's shared memory (rows of at most 64 tiles
+    of 8192 logits, at most 16,384 groups: tiles when there are at least 2W of
+    them, else their 128 sub-chunks each), else a row-statistics kernel too."""
+    n_tpr = -(-V // 8192)
+    n_tiles = W_in * n_tpr
+    n_groups = n_tiles if n_tiles >= 2 * W else n_tiles * 128
+    return 2 if (n_tpr <= 64 and n_groups <= 16384) else 3
+
+
 def decode_attn_bytes(W, Lp, L_prev, Hq, Hkv, D) -> float:
     row = Hkv * D * 2
     q_o = 2 * W * Hq * D * 2
@@ -350,7 +361,8 @@ def measure_decode_loop(dev, bw, seed, stop_id, stream, peaks, flush, reps=20, w
     from attention_packed_varlen_gb300 import _binding as slm
     slm.slm_check_status(loop.status)
     n = bw.steps
-    launches = 3 + 1 + n * (1 + 3 + 1) + ((n + 1) if stop_id is not None else 0)
+    launches = (select_launches(1, V, W) + 1 + n * (1 + select_launches(W, V, W) + 1)
+                + ((n + 1) if stop_id is not None else 0))
     nbytes = loop_bytes(bw)
     return {"stop_id": stop_id, "decode_steps": n, "graph_us_per_loop": graph_s * 1e6,
             "graph_us_per_decode_step": graph_s * 1e6 / n, "eager_us_per_loop": eager_s * 1e6,
@@ -776,8 +788,9 @@ def run_gpu(args):
         if not args.no_extra_legs:
             oracle_t = oracle_timings()
 
-    # prefill: schedule + attention; decode step: attention + 3 selection kernels
-    launches_per_step = n_pre * 2 + sum(n_dec) * 4
+    # prefill: schedule + attention; decode step: attention + the selection's kernels
+    launches_per_step = n_pre * 2 + sum(n_dec[j] * (1 + select_launches(b.w.beams, b.w.vocab, b.w.beams))
+                                        for j, b in enumerate(beams))
     peak_sust = peaks["bf16_tflops_sustained"]
     peak_burst = peaks["bf16_tflops"]
     clocks = clk.summary()

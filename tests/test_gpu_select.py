@@ -5,7 +5,9 @@ the oracle's own ranking explained by the normalisers' few-ulp difference.
 Two-stage candidate selection (article "SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化",
 section 3.3) on the two beam workloads at full size (V = 151,936), the first
 step (one row), heavy ties (few distinct logits, all-equal rows), a
-vocabulary that is not a multiple of 8, 2W = V, and W = 1.
+vocabulary that is not a multiple of 8, 2W = V, W = 1, rows long enough for
+the three-kernel path, and a dominant token that pushes the threshold far
+below the largest score.
 """
 import numpy as np
 import pytest
@@ -83,3 +85,31 @@ def test_sampled_threshold_miss():
     for b in range(W_in):
         logits[b, runs] = 20.0
     run_and_check(logits, s.cum, W)
+
+
+@pytest.mark.parametrize("W_in,V,W", [(2, 600000, 2), (1, 600000, 50)])
+def test_long_rows_three_kernel_path(W_in, V, W):
+    # Rows of more than 64 tiles of 8192 take the path with the separate
+    # row-statistics kernel and the global histogram: tile groups (2 rows,
+    # 4 candidates) and sub-chunk groups (one row, 100 candidates).
+    s = wl.select_inputs(W_in, V, W, seed=V + W_in)
+    run_and_check(s.logits, s.cum, W)
+
+
+@pytest.mark.parametrize("W_in,W", [(1, 100), (100, 100)])
+def test_dominant_token_threshold_far_below_top(W_in, W):
+    # One logit per row far above the rest, and a zero cumulative score for
+    # beam 0: its candidate scores exactly 0 (the log-normaliser rounds to
+    # the dominant logit), while the 2W-th group key lies near -50, dozens of
+    # binades further down and outside the select kernel's shared histogram
+    # window, so the threshold is taken by exact radix selection instead.
+    V = 151936
+    s = wl.select_inputs(W_in, V, W, seed=31 + W_in, step=0 if W_in == 1 else 1)
+    logits = s.logits.clone()
+    cols = torch.arange(W_in) * 997 % V
+    logits[torch.arange(W_in), cols] = 60.0
+    cum = s.cum.clone()
+    cum[0] = 0.0
+    res, _ = run_and_check(logits, cum, W)
+    kept = set(zip(res["parent"].cpu().tolist(), res["token"].cpu().tolist()))
+    assert all((b, int(cols[b])) in kept for b in range(W_in))
