@@ -497,43 +497,34 @@ struct Scratch {
   unsigned long long wu64[2][kSelWarps];
   int wint[kSelWarps];
   uint32_t wkey[kSelWarps];
-  int digit, above, in_bin, counter, flag, dstar, total;
+  int digit, above, in_bin, counter, flag, dstar;
   unsigned long long u64;
 };
 
-// Block-wide exclusive prefix sum and total.  The warps' totals are scanned
-// by warp 0 alone: every thread then reads two words of shared memory, where
-// a loop over the 32 warp totals in every thread costs ~1,000 cycles of the
-// shared-memory pipe.
+// Block-wide exclusive prefix sum and total.  After one barrier every warp
+// reads the warps' totals, one word per lane, and scans them with shuffles:
+// two barriers, and no thread loops over the 32 totals (which costs ~1,000
+// cycles of the shared-memory pipe per call with 1024 threads).
 __device__ __forceinline__ int block_scan_excl(int v, int* total, Scratch& sh) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int x = warp_inclusive_scan(v, lane);
-  __syncthreads();
+  __syncthreads();  // earlier readers of sh.wint are done
   if (lane == 31) sh.wint[w] = x;
   __syncthreads();
-  if (w == 0) {
-    const int y = (lane < kSelWarps) ? sh.wint[lane] : 0;
-    const int inc = warp_inclusive_scan(y, lane);
-    sh.wint[lane] = inc - y;
-    if (lane == 31) sh.total = inc;
-  }
-  __syncthreads();
-  *total = sh.total;
-  return sh.wint[w] + x - v;
+  const int y = (lane < kSelWarps) ? sh.wint[lane] : 0;
+  const int inc = warp_inclusive_scan(y, lane);
+  *total = __shfl_sync(kFull, inc, 31);
+  return __shfl_sync(kFull, inc - y, w) + x - v;
 }
 
-// Block-wide maximum (warp 0 reduces the warps' maxima).
+// Block-wide maximum (two barriers, as above).
 __device__ __forceinline__ uint32_t block_max_u32(uint32_t v, Scratch& sh) {
+  const int lane = threadIdx.x & 31;
   v = warp_max_u32(v);
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) sh.wkey[threadIdx.x >> 5] = v;
+  if (lane == 0) sh.wkey[threadIdx.x >> 5] = v;
   __syncthreads();
-  if (threadIdx.x < 32) {
-    const uint32_t r = warp_max_u32((threadIdx.x < kSelWarps) ? sh.wkey[threadIdx.x] : 0u);
-    if (threadIdx.x == 0) sh.wkey[0] = r;
-  }
-  __syncthreads();
-  return sh.wkey[0];
+  return warp_max_u32((lane < kSelWarps) ? sh.wkey[lane] : 0u);
 }
 
 // k-th largest (1-based, counting repeats) of the 64-bit keys all threads
@@ -878,7 +869,6 @@ __device__ bool fused_threshold(const SelSmem& sm, int* hist, int n_groups, int 
   }
   __syncthreads();
   const int dstar = sh.dstar;
-  __syncthreads();
   if (dstar < 0) return false;
   *Lk = (top - static_cast<uint32_t>(dstar)) << 16;
   return true;
