@@ -27,14 +27,14 @@
 // 2. select (one CTA per SM, a programmatic dependent of the stream): every
 //    CTA derives lse_b of every beam from the tile partials (a thread per
 //    beam, its tiles in order) and every group's best score key into shared
-//    memory, radix-selects the 2W-th largest key as L, lists the groups
-//    scoring >= L in group order, and takes its share of them: it reads
-//    their sub-chunks scoring >= L back from the logits and appends the
-//    logits scoring >= L to a small list.  The last CTA to finish ranks that
-//    list with the full order (score bins, then pairwise within a bin) and
-//    writes the 2W results.  If the list would overflow (huge score ties)
-//    the last CTA ranks every logit scoring >= L exactly with a radix select
-//    instead.
+//    memory, and takes as L the lower edge of the bin of 2^16 keys holding
+//    the 2W-th largest key (a shared histogram); warp w of the grid then
+//    re-reads, of the groups w, w + n_warps, ..., those scoring >= L -- their
+//    sub-chunks scoring >= L -- and appends the logits scoring >= L to a
+//    small list.  The last CTA to finish ranks that list with the full order
+//    (score bins, then pairwise within a bin) and writes the 2W results.  If
+//    the list would overflow (huge score ties) the last CTA ranks every logit
+//    scoring >= L exactly with a radix select instead.
 //
 // Shapes whose group keys do not fit the select kernel's shared memory (more
 // than 16,384 groups, or rows of more than 64 tiles) run a row-statistics
@@ -929,107 +929,78 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
     if (sh.dstar >= 0) Lk = static_cast<uint32_t>(sh.dstar) << 16;
   }
 
-  // the groups scoring >= L, in group order (every CTA builds the same list
-  // and takes its share of it): each warp reads a contiguous range once,
-  // keeping one ballot word per 32 groups in shared memory
-  int n_found;
+  // Read back the groups scoring >= L and append their logits scoring >= L.
+  // Warp gw of the grid takes groups gw, gw + n_gw, gw + 2 n_gw, ...: each
+  // lane tests one group's key per step and the warp re-reads the groups that
+  // pass one by one, so the ~2W groups spread over the grid's warps without a
+  // shared list.  Per group, a warp handles up to four of its sub-chunks
+  // scoring >= L at once, eight lanes each, one 16-byte run of eight logits
+  // per lane.
+  auto group_key = [&](int g) -> uint32_t { return kFused ? sm.keys[g] : __ldcg(p.gkeys + g); };
   {
-    uint32_t* words = sm.u.words;
-    const int n_words = min((n_groups + 31) >> 5, kUnitWords);  // more groups: the exact path
-    const int per = (n_words + kSelWarps - 1) / kSelWarps;  // words per warp
-    const int w_lo = min(n_words, warp * per), w_hi = min(n_words, w_lo + per);
-    int cnt = 0;
-    for (int w0 = w_lo; w0 < w_hi; w0 += 8) {
-      uint32_t k8[8];
+    const int gw = blockIdx.x * kSelWarps + warp, n_gw = gridDim.x * kSelWarps;
+    for (int g0 = gw; g0 < n_groups; g0 += 32 * n_gw) {
+      const int gl = g0 + lane * n_gw;
+      unsigned pending = __ballot_sync(kFull, gl < n_groups && group_key(gl) >= Lk);
+      while (pending) {
+        const int g = g0 + (__ffs(pending) - 1) * n_gw;
+        pending &= pending - 1u;
+        const int t = tile_level ? g : g / kSubPerTile;
+        const int b = t / nt, c = t - b * nt;
+        const float cum = sm.cum[b], lse = sm.lse[b];
+        // the tile's sub-chunks scoring >= L, as four lane masks (q = 0..3)
+        unsigned mq[kQuarters];
+        if (tile_level) {
+          const uint16_t* smx = p.submax + static_cast<int64_t>(t) * kSubPerTile;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int g = (w0 + i) * 32 + lane;
-        k8[i] = (w0 + i < w_hi && g < n_groups) ? (kFused ? sm.keys[g] : __ldcg(p.gkeys + g)) : 0u;
-      }
+          for (int q = 0; q < kQuarters; ++q)
+            mq[q] = __ballot_sync(kFull, score_key_x(bf16_bits_to_f32(__ldcg(smx + q * 32 + lane)), cum, lse) >= Lk);
+        } else {
+          const int s = g - t * kSubPerTile;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int g = (w0 + i) * 32 + lane;
-        const unsigned bal = __ballot_sync(kFull, w0 + i < w_hi && g < n_groups && k8[i] >= Lk);
-        if (w0 + i < w_hi && lane == 0) words[w0 + i] = bal;
-        cnt += __popc(bal);
-      }
-    }
-    // the warps' counts in warp order: lane 0 of each warp contributes its count
-    int pos = block_scan_excl(lane == 0 ? cnt : 0, &n_found, sh);
-    pos = __shfl_sync(kFull, pos, 0);
-    for (int wd = w_lo; wd < w_hi; ++wd) {
-      const unsigned bal = words[wd];
-      const int at = pos + __popc(bal & ((1u << lane) - 1u));
-      if (((bal >> lane) & 1u) && at < kUnitCap) sm.units[at] = wd * 32 + lane;
-      pos += __popc(bal);
-    }
-    __syncthreads();
-  }
-  const int n_units = min(n_found, kUnitCap);
-  const bool unit_over = n_found > kUnitCap || ((n_groups + 31) >> 5) > kUnitWords;
-
-  // Read back this CTA's share of the sub-chunks scoring >= L and append their
-  // logits scoring >= L.  A warp handles up to four sub-chunks at once, eight
-  // lanes each, one 16-byte run of eight logits per lane.
-  if (!unit_over) {
-    const int wg = blockIdx.x * kSelWarps + warp, n_wg = gridDim.x * kSelWarps;
-    for (int u = wg; u < n_units; u += n_wg) {
-      const int g = sm.units[u];
-      const int t = tile_level ? g : g / kSubPerTile;
-      const int b = t / nt, c = t - b * nt;
-      const float cum = sm.cum[b], lse = sm.lse[b];
-      // the tile's sub-chunks scoring >= L, as four lane masks (q = 0..3)
-      unsigned mq[kQuarters];
-      if (tile_level) {
-        const uint16_t* smx = p.submax + static_cast<int64_t>(t) * kSubPerTile;
-#pragma unroll
-        for (int q = 0; q < kQuarters; ++q)
-          mq[q] = __ballot_sync(kFull, score_key_x(bf16_bits_to_f32(__ldcg(smx + q * 32 + lane)), cum, lse) >= Lk);
-      } else {
-        const int s = g - t * kSubPerTile;
-#pragma unroll
-        for (int q = 0; q < kQuarters; ++q) mq[q] = (q == s / 32) ? (1u << (s % 32)) : 0u;
-      }
-      const int n0 = __popc(mq[0]), n1 = __popc(mq[1]), n2 = __popc(mq[2]);
-      const int n_sub = n0 + n1 + n2 + __popc(mq[3]);
-      for (int base = 0; base < n_sub; base += 4) {
-        const int j = base + (lane >> 3), r = lane & 7;  // sub-chunk j of the list, run r
-        int cnt = 0;
-        uint4 x = make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
-        int col = 0;
-        if (j < n_sub) {
-          int q = 0, k = j;
-          unsigned m = mq[0];
-          if (k >= n0) { k -= n0; q = 1; m = mq[1];
-            if (k >= n1) { k -= n1; q = 2; m = mq[2];
-              if (k >= n2) { k -= n2; q = 3; m = mq[3]; } } }
-          for (int i = 0; i < k; ++i) m &= m - 1u;  // drop the k lowest set bits
-          const int l = __ffs(m) - 1;
-          col = c * kTile + sub_run_offset(q, l, r);
-          x = load_run(p, b, col);
+          for (int q = 0; q < kQuarters; ++q) mq[q] = (q == s / 32) ? (1u << (s % 32)) : 0u;
         }
-        const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
-        uint32_t keys[8];
+        const int n0 = __popc(mq[0]), n1 = __popc(mq[1]), n2 = __popc(mq[2]);
+        const int n_sub = n0 + n1 + n2 + __popc(mq[3]);
+        for (int base = 0; base < n_sub; base += 4) {
+          const int j = base + (lane >> 3), r = lane & 7;  // sub-chunk j of the list, run r
+          int cnt = 0;
+          uint4 x = make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
+          int col = 0;
+          if (j < n_sub) {
+            int q = 0, k = j;
+            unsigned m = mq[0];
+            if (k >= n0) { k -= n0; q = 1; m = mq[1];
+              if (k >= n1) { k -= n1; q = 2; m = mq[2];
+                if (k >= n2) { k -= n2; q = 3; m = mq[3]; } } }
+            for (int i = 0; i < k; ++i) m &= m - 1u;  // drop the k lowest set bits
+            const int l = __ffs(m) - 1;
+            col = c * kTile + sub_run_offset(q, l, r);
+            x = load_run(p, b, col);
+          }
+          const uint32_t wd[4] = {x.x, x.y, x.z, x.w};
+          uint32_t keys[8];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          keys[h] = score_key_x(bf16_bits_to_f32((h & 1) ? (wd[h >> 1] >> 16) : (wd[h >> 1] & 0xFFFFu)), cum, lse);
-          cnt += (j < n_sub && keys[h] >= Lk);
-        }
-        const int incl = warp_inclusive_scan(cnt, lane);
-        const int total = __shfl_sync(kFull, incl, 31);
-        if (total == 0) continue;
-        unsigned pos0 = 0;
-        if (lane == 0) pos0 = atomicAdd(p.misc + kMiscCand, static_cast<unsigned>(total));
-        int pos = static_cast<int>(__shfl_sync(kFull, pos0, 0)) + incl - cnt;
+          for (int h = 0; h < 8; ++h) {
+            keys[h] = score_key_x(bf16_bits_to_f32((h & 1) ? (wd[h >> 1] >> 16) : (wd[h >> 1] & 0xFFFFu)), cum, lse);
+            cnt += (j < n_sub && keys[h] >= Lk);
+          }
+          const int incl = warp_inclusive_scan(cnt, lane);
+          const int total = __shfl_sync(kFull, incl, 31);
+          if (total == 0) continue;
+          unsigned pos0 = 0;
+          if (lane == 0) pos0 = atomicAdd(p.misc + kMiscCand, static_cast<unsigned>(total));
+          int pos = static_cast<int>(__shfl_sync(kFull, pos0, 0)) + incl - cnt;
 #pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          if (j < n_sub && keys[h] >= Lk) {
-            if (pos < kCandCap) {
-              const uint32_t bits = (h & 1) ? (wd[h >> 1] >> 16) : (wd[h >> 1] & 0xFFFFu);
-              p.cand[pos] = global_entry(keys[h], static_cast<uint32_t>(b),
-                                         cand_entry(bits, static_cast<uint32_t>(col + h)));
+          for (int h = 0; h < 8; ++h) {
+            if (j < n_sub && keys[h] >= Lk) {
+              if (pos < kCandCap) {
+                const uint32_t bits = (h & 1) ? (wd[h >> 1] >> 16) : (wd[h >> 1] & 0xFFFFu);
+                p.cand[pos] = global_entry(keys[h], static_cast<uint32_t>(b),
+                                           cand_entry(bits, static_cast<uint32_t>(col + h)));
+              }
+              ++pos;
             }
-            ++pos;
           }
         }
       }
@@ -1050,7 +1021,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
     return;
   }
   const int n_cand = static_cast<int>(__ldcg(p.misc + kMiscCand));
-  if (!unit_over && n_cand <= kCandCap) {
+  if (n_cand <= kCandCap) {
     if (n_cand < K) {  // cannot happen: every group scoring >= L holds one candidate
       write_errors(p, sm);
       return;
@@ -1117,14 +1088,52 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
   }
 
   // Huge score ties: every logit scoring >= L, ranked exactly.  The groups
-  // scoring >= L are found again (the list may have overflowed), and all of
-  // their logits are visited.
+  // scoring >= L are listed in group order (each warp reads a contiguous
+  // range once, keeping one ballot word per 32 groups in shared memory) or,
+  // when they overflow the list, every group is tested; all of their logits
+  // are visited.
+  int n_found;
+  {
+    uint32_t* words = sm.u.words;
+    const int n_words = min((n_groups + 31) >> 5, kUnitWords);  // more groups: the exact path
+    const int per = (n_words + kSelWarps - 1) / kSelWarps;  // words per warp
+    const int w_lo = min(n_words, warp * per), w_hi = min(n_words, w_lo + per);
+    int cnt = 0;
+    for (int w0 = w_lo; w0 < w_hi; w0 += 8) {
+      uint32_t k8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int g = (w0 + i) * 32 + lane;
+        k8[i] = (w0 + i < w_hi && g < n_groups) ? group_key(g) : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int g = (w0 + i) * 32 + lane;
+        const unsigned bal = __ballot_sync(kFull, w0 + i < w_hi && g < n_groups && k8[i] >= Lk);
+        if (w0 + i < w_hi && lane == 0) words[w0 + i] = bal;
+        cnt += __popc(bal);
+      }
+    }
+    // the warps' counts in warp order: lane 0 of each warp contributes its count
+    int pos = block_scan_excl(lane == 0 ? cnt : 0, &n_found, sh);
+    pos = __shfl_sync(kFull, pos, 0);
+    for (int wd = w_lo; wd < w_hi; ++wd) {
+      const unsigned bal = words[wd];
+      const int at = pos + __popc(bal & ((1u << lane) - 1u));
+      if (((bal >> lane) & 1u) && at < kUnitCap) sm.units[at] = wd * 32 + lane;
+      pos += __popc(bal);
+    }
+    __syncthreads();
+  }
+  const int n_units = min(n_found, kUnitCap);
+  const bool unit_over = n_found > kUnitCap || ((n_groups + 31) >> 5) > kUnitWords;
+
   const int group_size = tile_level ? kTile : 64;
   const int n_scan = unit_over ? n_groups : n_units;
   auto for_each_entry = [&](auto f) {
     for (int u = 0; u < n_scan; ++u) {
       const int g = unit_over ? u : sm.units[u];
-      if (unit_over && (kFused ? sm.keys[g] : __ldcg(p.gkeys + g)) < Lk) continue;  // uniform: the same key
+      if (unit_over && group_key(g) < Lk) continue;  // uniform: every thread tests the same key
       const int t = tile_level ? g : g / kSubPerTile;
       const int b = t / nt, c = t - b * nt;
       const float cum = sm.cum[b], lse = sm.lse[b];
