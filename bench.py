@@ -291,6 +291,15 @@ def run_decode_step(slm_lib, bs: BeamSet, t: int, stream_ptr):
         None, None, P(bs.dec_ws), bs.dec_ws.numel(), stream_ptr)
     if st != 0:
         raise RuntimeError(slm_lib.slm_last_error().decode())
+    run_select(slm_lib, bs, t, stream_ptr)
+
+
+def run_select(slm_lib, bs: BeamSet, t: int, stream_ptr):
+    """The step's beam selection over its fresh logits [W, V]."""
+    import ctypes
+    bw = bs.w
+    logits = bs.steps[t][4]
+    P = lambda x: ctypes.c_void_p(x.data_ptr())
     r = bs.res
     st = slm_lib.slm_beam_select(
         P(logits), P(bs.cum), bw.beams, bw.vocab, bw.beams, P(r["token"]), P(r["parent"]), P(r["score"]),
@@ -848,6 +857,11 @@ def run_ncu_case(args):
         ps = PrefillSet(dev, 1, PREFILL_SEED)   # one layer of the 240-sequence batch (1.6 GB)
         for _ in range(3):
             run_prefill_layer(lib, ps, ps.layers[0], sp)
+    elif args.ncu_case == "select":  # stream + select of the W=400 selection (121.5 MB of logits)
+        bw = wl.LONG_PROMPT_WIDE_BEAM
+        bs = BeamSet(dev, bw, wl.workload_seed(5))
+        for _ in range(3):
+            run_select(lib, bs, bw.steps - 1, sp)
     else:
         bw = wl.LONG_PROMPT_WIDE_BEAM
         bs = BeamSet(dev, bw, wl.workload_seed(5))
@@ -870,7 +884,7 @@ def main():
                     help="skip the decode-loop graph and head-kernel timings")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per prefill launch from an ncu capture of the current kernel")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "select"], default=None,
                     help="run one kernel on a reduced input for an ncu capture, then exit")
     args = ap.parse_args()
     if args.ncu_case:
