@@ -139,13 +139,13 @@ cudaError_t launch_attn(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   cfg.blockDim = dim3(kFwdThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
+  // a programmatic dependent of the kernel before it (prefill: the schedule
+  // kernel launched just before); the kernel waits before reading memory
   cudaLaunchAttribute attr[1];
-  if constexpr (MODE == AttnMode::kPrefill) {  // overlaps the schedule kernel launched just before
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, to, p);
 }
 

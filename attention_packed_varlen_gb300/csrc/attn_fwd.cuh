@@ -26,8 +26,9 @@
 // maximum until a block raises it by more than 2^8 (the factor cancels in the
 // final division), so O is rarely rescaled.
 //
-// Prefill runs as a programmatic dependent of its schedule kernel (setup
-// first, griddepcontrol.wait before the work items are read).  Decode can
+// The kernel runs as a programmatic dependent of the one before it (prefill:
+// its schedule kernel): setup first, griddepcontrol.wait before any global
+// memory is read.  Decode can
 // split the prompt's key blocks over several CTAs per beam tile: each split
 // leaves its rows' partial softmax state in a caller workspace and the last
 // one to finish (atomic ticket) merges them before the suffix keys.
@@ -292,10 +293,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  // Prefill runs as a programmatic dependent of its schedule kernel: the
-  // setup above overlaps it, the work items are read only after this.  A CTA
-  // beyond the last unit runs empty loops and frees its TMEM.
-  if constexpr (MODE == AttnMode::kPrefill) pdl_wait();
+  // A programmatic dependent of the kernel before it (prefill: its schedule
+  // kernel): the setup above overlaps that kernel, global memory is read only
+  // after this.  A CTA beyond the last unit runs empty loops and frees its
+  // TMEM.
+  pdl_wait();
+  pdl_launch_dependents();
   const int n_units = (MODE == AttnMode::kPrefill) ? num_units<MODE>(p) : n_units_dec;
 
   if (warp == 8) {

@@ -473,9 +473,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     }
     sh.abort = 0;
     fence_mbarrier_init();
-    if (blockIdx.x == 0)
-      for (int i = 0; i < kMiscWords; ++i) p.misc[i] = 0u;  // read by the select kernel after this grid ends
   }
+  // Global memory (the logits, and the workspace an earlier call's select
+  // kernel reads) only after everything before this kernel is done; as an
+  // ordinary launch it starts after that anyway, and the wait returns at once.
+  grid_dep_wait();
+  if (threadIdx.x == 0 && blockIdx.x == 0)
+    for (int i = 0; i < kMiscWords; ++i) p.misc[i] = 0u;  // read by the select kernel after this grid ends
   if (!p.fused) {  // this CTA's slice of the group-key histogram (filled by the row kernel after this grid ends)
     const int per = (kHistBins + gridDim.x - 1) / gridDim.x;
     const int end = min(kHistBins, (static_cast<int>(blockIdx.x) + 1) * per);
@@ -881,13 +885,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
   Scratch& sh = sm.sc;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int K = p.K, nt = p.n_tpr;
-  // inputs that do not come from the previous kernels: before the wait
-  for (int b = tid; b < p.W_in; b += kSelThreads) sm.cum[b] = __ldg(p.cum + b);
   for (int i = tid; i < kBins; i += kSelThreads) {
     sm.bins[i] = 0u;
     sm.fill[i] = 0;
   }
+  // Global memory only after the wait: the stream kernel's products, and the
+  // cumulative scores, which an earlier kernel still running may be writing.
   grid_dep_wait();
+  for (int b = tid; b < p.W_in; b += kSelThreads) sm.cum[b] = __ldcg(p.cum + b);
   // the groups: tiles when there are at least K of them, else sub-chunks
   const bool tile_level = p.n_tiles >= K;
   const int n_groups = tile_level ? p.n_tiles : p.n_tiles * kSubPerTile;
@@ -1014,6 +1019,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const Params p) 
     sh.flag = (atom_add_acq_rel(p.misc + kMiscTicket, 1u) == gridDim.x - 1);
   }
   __syncthreads();
+  grid_dep_launch();  // the next kernel may start its setup while the last CTA ranks
   if (!sh.flag) return;
 
   if (__ldcg(p.misc + kMiscStatus) != 0u) {
@@ -1278,17 +1284,13 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   p.out_cand_score = out_cand_score;
   p.out_lse = out_lse;
 
-  // The stream kernel is an ordinary launch: it starts after everything
-  // before it on the stream, including a previous call reading this workspace.
-  const size_t smem_stream = sizeof(sel::StreamSmem);
-  cudaError_t e = cudaFuncSetAttribute(sel::stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem_stream));
-  if (e != cudaSuccess) return e;
-  const int grid_stream = std::min(sm_count(), p.n_tiles);
-  sel::stream_kernel<<<grid_stream, sel::kStreamThreads, smem_stream, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
+  // The stream kernel is an ordinary launch: it starts once everything before
+  // it on the stream is done, a previous call still reading this workspace
+  // included (launched as a programmatic dependent of a decode attention, its
+  // 152 early CTAs held the SMs the attention leaves free and the W = 400
+  // decode loop ran 6 us slower).  The kernels after it are programmatic
+  // dependents: each sets itself up early and waits (griddepcontrol.wait)
+  // before it touches global memory.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1296,6 +1298,18 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const size_t smem_stream = sizeof(sel::StreamSmem);
+  cudaError_t e = cudaFuncSetAttribute(sel::stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem_stream));
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(std::min(sm_count(), p.n_tiles));
+  cfg.blockDim = dim3(sel::kStreamThreads);
+  cfg.dynamicSmemBytes = smem_stream;
+  cfg.numAttrs = 0;
+  e = cudaLaunchKernelEx(&cfg, sel::stream_kernel, p);
+  if (e != cudaSuccess) return e;
+  cfg.numAttrs = 1;
+
   if (!p.fused) {
     cfg.gridDim = dim3(p.n_tiles < p.K ? W_in : (W_in + sel::kRowWarps - 1) / sel::kRowWarps);
     cfg.blockDim = dim3(sel::kRowThreads);

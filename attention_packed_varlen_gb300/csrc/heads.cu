@@ -20,6 +20,7 @@
 #include <cuda_runtime.h>
 
 #include "slm_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace slm {
 namespace heads {
@@ -257,6 +258,8 @@ __global__ void __launch_bounds__(kFinThreads) beam_finished_kernel(
     carry_a = 0;
     carry_f = 0;
   }
+  pdl_wait();  // a programmatic dependent of the selection: its results are complete
+  pdl_launch_dependents();
   __syncthreads();
   for (int i0 = 0; i0 < 2 * W; i0 += kFinThreads) {
     const int i = i0 + tid;
@@ -311,6 +314,8 @@ __global__ void __launch_bounds__(kFinThreads) beam_finished_kernel(
 __global__ void beam_history_kernel(const int32_t* __restrict__ hin, const int32_t* __restrict__ parent,
                                     const int32_t* __restrict__ token, int W, int W_in, int t, int max_len,
                                     int32_t* __restrict__ hout, int32_t* dev_status) {
+  pdl_wait();  // a programmatic dependent of the kernel before it: its outputs are complete
+  pdl_launch_dependents();
   const int b = blockIdx.x;
   int src = parent ? parent[b] : b;
   if (t > 0 && (src < 0 || src >= W_in)) {  // at t = 0 no row is gathered
@@ -355,17 +360,19 @@ cudaError_t launch_beam_finished(const int32_t* cand_token, const int32_t* cand_
                                  int32_t* fin_token, int32_t* fin_parent, float* fin_score, int32_t* fin_count,
                                  cudaStream_t stream) {
   using namespace heads;
-  beam_finished_kernel<<<1, kFinThreads, 0, stream>>>(cand_token, cand_parent, cand_score, W, stop_id, out_token,
-                                                      out_parent, out_score, fin_token, fin_parent, fin_score,
-                                                      fin_count);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(attr, dim3(1), dim3(kFinThreads), stream);
+  return cudaLaunchKernelEx(&cfg, beam_finished_kernel, cand_token, cand_parent, cand_score, W, stop_id, out_token,
+                            out_parent, out_score, fin_token, fin_parent, fin_score, fin_count);
 }
 
 cudaError_t launch_beam_history(const int32_t* hist_in, const int32_t* parent, const int32_t* token, int W, int W_in,
                                 int t, int max_len, int32_t* hist_out, int32_t* dev_status, cudaStream_t stream) {
   using namespace heads;
-  beam_history_kernel<<<W, 32, 0, stream>>>(hist_in, parent, token, W, W_in, t, max_len, hist_out, dev_status);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(attr, dim3(W), dim3(32), stream);
+  return cudaLaunchKernelEx(&cfg, beam_history_kernel, hist_in, parent, token, W, W_in, t, max_len, hist_out,
+                            dev_status);
 }
 
 }  // namespace slm

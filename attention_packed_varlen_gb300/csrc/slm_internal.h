@@ -2,8 +2,26 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_runtime.h>
 
 namespace slm {
+
+// Launch configuration for a programmatic dependent of the kernel before it
+// on the stream (griddepcontrol.wait in the kernel orders its memory accesses
+// after that kernel; its setup may overlap that kernel's tail).
+inline cudaLaunchConfig_t pdl_config(cudaLaunchAttribute* attr, dim3 grid, dim3 block, cudaStream_t stream,
+                                     size_t smem = 0) {
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
 
 // Bits of the device status word (int32) that kernels OR into *dev_status.
 constexpr int32_t kDevBadSeqlens = 1;        // sequence boundary not non-decreasing / not ending at T
