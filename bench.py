@@ -174,7 +174,7 @@ class ClockSampler:
 # capture of `bench.py --ncu-case prefill` (one layer of the same batch), keyed
 # by the code it was taken on (the kernel, its PTX helpers and the host launch,
 # comments and blank space left out); any other code reports null.
-PREFILL_TRAFFIC = {"1f260d39c47cd5ef": 1.191185e9 + 0.512354e9}
+PREFILL_TRAFFIC = {"12fba8de95f366fe": 1.199149e9 + 0.512910e9}
 
 
 def prefill_code_key() -> str:
