@@ -72,7 +72,7 @@ constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kRowThreads = 256;                   // row-statistics kernel: a warp per beam
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kMaxRows = 1024;                     // W_in limit
-constexpr int kUnitCap = 8192;                     // groups the normal path lists
+constexpr int kUnitCap = 8192;                     // groups the exact path lists (more: it tests every group)
 constexpr int kCandCap = 4096;                     // candidates the final sort holds
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kNegInf2 = 0xFF80FF80u;         // two bf16 -inf
@@ -718,14 +718,13 @@ constexpr int kUnitWords = 16384;                // ballot words: groups up to 5
 constexpr int kBinsPerThread = kBins / kSelThreads;
 constexpr int kCandPer = kCandCap / kSelThreads;  // candidates per thread in the final ranking
 static_assert(kBins % kSelThreads == 0, "whole bins per thread");
-static_assert(kUnitCap >= kCandCap, "the final ranking's order fits the group list");
 
 // Dynamic shared memory of the select kernel.
 struct SelSmem {
   float lse[kMaxRows];
   float cum[kMaxRows];
   uint32_t keys[kKeyCap];     // fused path: every group's best score key
-  int units[kUnitCap];        // groups scoring >= L (tiles, or sub-chunks t * 128 + s); the final ranking's lists
+  int units[kUnitCap];        // the exact path: groups scoring >= L (tiles, or sub-chunks t * 128 + s)
   unsigned bins[kBins];
   int fill[kBins];
   int rtok[2048], rpar[2048];  // the K results, written out together
