@@ -55,3 +55,20 @@ def test_loop_bytes_sum_its_steps():
         bench.decode_attn_bytes(bw.beams, bw.prefix_len, t, bw.n_q_heads, bw.n_kv_heads, bw.head_dim)
         + bw.beams * 151936 * 2 for t in range(bw.steps))
     assert bench.loop_bytes(bw) == want
+
+
+def test_selection_launch_count_follows_the_fused_path():
+    # stream + select while the group keys fit the select kernel's shared
+    # memory (rows of at most 64 tiles of 8192, at most 16,384 groups); a
+    # row-statistics kernel in between otherwise
+    assert bench.select_launches(100, 151936, 100) == 2      # 1,900 tile groups
+    assert bench.select_launches(400, 151936, 400) == 2      # 7,600 tile groups
+    assert bench.select_launches(1, 151936, 400) == 2        # 19 tiles < 2W: 2,432 sub-chunk groups
+    assert bench.select_launches(900, 151936, 200) == 3      # 17,100 tile groups
+    assert bench.select_launches(8, 151936, 100) == 3        # 152 tiles < 2W: 19,456 sub-chunk groups
+    assert bench.select_launches(2, 600000, 2) == 3          # 74 tiles per row
+    # the loops' launch counts: first step (selection + history), then per
+    # step attention + selection + history
+    bw = wl.LONG_PROMPT_WIDE_BEAM
+    per_step = 1 + bench.select_launches(bw.beams, bw.vocab, bw.beams) + 1
+    assert bench.select_launches(1, bw.vocab, bw.beams) + 1 + bw.steps * per_step == 23
