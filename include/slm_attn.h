@@ -16,6 +16,10 @@
  *     the call returns.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream) and never synchronise, except slm_check_status.
+ *     Stream order holds as usual; most kernels are launched as programmatic
+ *     dependents of the kernel before them, so their set-up (barriers,
+ *     tensor memory) may overlap it, but none reads or writes global memory
+ *     before everything earlier on the stream has completed.
  *   - Arguments that can be checked on the host are; a bad one returns a
  *     status other than SLM_OK, sets a thread-local message readable with
  *     slm_last_error(), and enqueues nothing.  No call throws, aborts or traps.
