@@ -184,24 +184,35 @@ def test_graph_replay_equals_eager_and_takes_new_inputs(stop_id):
                                    b.view(torch.int16) if b.dtype == torch.bfloat16 else b), key
 
 
-def test_graph_replays_repeat_the_same_beams():
+@pytest.mark.parametrize("stop_id", [None, STOP])
+def test_graph_replays_repeat_the_same_beams(stop_id):
     # Many replays of the wide-beam loop: every selection, history and
     # reordered suffix must repeat bit for bit (the logits are inputs, so
     # nothing upstream of a selection varies), and the attention output may
     # differ only by the key-split merge's fp32 summation order.  A race in
-    # any kernel's pipeline would show up here as a replay that differs.
+    # any kernel's pipeline, or between kernels that start their setup while
+    # the one before still runs, would show up here as a replay that differs.
     bw = wl.LONG_PROMPT_WIDE_BEAM
-    d = wl.decode_loop_inputs(bw, 21)
+    d = wl.decode_loop_inputs(bw, 21, stop_id=stop_id, stop_rows=0.3 if stop_id is not None else 0.0)
     static = to_dev(d)
-    loop = make_loop(bw, None)
+    loop = make_loop(bw, stop_id)
     loop.record(*static)
     torch.cuda.synchronize()
     loop.capture(*static)
     loop.replay()
     torch.cuda.synchronize()
     first = snapshot(loop)
-    for _ in range(30):
+    ref = [{k: v.clone() for k, v in sel.items()} for sel in loop.sel]
+    ref_hist = [h.clone() for h in loop.hist]
+    for r in range(200):
         loop.replay()
+        if r % 10 == 9:  # compared on the device every tenth replay
+            torch.cuda.synchronize()
+            for a, b in zip(loop.sel, ref):
+                for k in a:
+                    assert torch.equal(a[k], b[k]), ("replay", r, k)
+            for a, b in zip(loop.hist, ref_hist):
+                assert torch.equal(a, b), ("replay", r, "hist")
     torch.cuda.synchronize()
     slm.slm_check_status(loop.status)
     last = snapshot(loop)
@@ -212,6 +223,10 @@ def test_graph_replays_repeat_the_same_beams():
     for a, b in zip(first["sel"], last["sel"]):
         for k in a:
             assert torch.equal(a[k], b[k]), ("sel", k)
+    if stop_id is not None:
+        for a, b in zip(first["fin"], last["fin"]):
+            for k in a:
+                assert torch.equal(a[k], b[k]), ("fin", k)
     for a, b in zip(first["o"], last["o"]):
         gap = (a.float() - b.float()).abs()
         lim = torch.maximum(a.float().abs(), b.float().abs()) * 2.0 ** -7 + 2.0 ** -20
