@@ -103,10 +103,6 @@ __device__ __forceinline__ uint32_t bf16_key(uint32_t bits) {
   return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
 }
 
-__device__ __forceinline__ uint32_t key_to_bf16(uint32_t key) {
-  return (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
-}
-
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits) { return __uint_as_float((bits & 0xFFFFu) << 16); }
 
 __device__ __forceinline__ uint32_t f32_key(float f) {
@@ -119,20 +115,9 @@ __device__ __forceinline__ float key_to_f32(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// Beam-local key: larger = earlier (higher logit, then lower id).
-__device__ __forceinline__ unsigned long long local_key(uint32_t key16, uint32_t token) {
-  return (static_cast<unsigned long long>(key16) << 32) | (0xFFFFFFFFu - token);
-}
-
 // A candidate as stored: bf16 bits in 32..47, token id in 0..31.
 __device__ __forceinline__ unsigned long long cand_entry(uint32_t bits, uint32_t token) {
   return (static_cast<unsigned long long>(bits & 0xFFFFu) << 32) | token;
-}
-
-// Score key of a candidate of beam b: fl32(cum + fl32(x - lse)), order-preserving.
-__device__ __forceinline__ uint32_t score_key(unsigned long long e, float cum, float lse) {
-  const float x = bf16_bits_to_f32(static_cast<uint32_t>(e >> 32));
-  return f32_key(__fadd_rn(cum, __fsub_rn(x, lse)));
 }
 
 // Global order as a 128-bit key (hi, lo), larger = earlier: score, then lower
