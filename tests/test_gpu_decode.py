@@ -61,7 +61,7 @@ def check_step(d, ks_host, vs_host, o, lse, ks_out, vs_out, what, with_new=True,
                                                 absv(args[1]), *args[2:], n_threads=THREADS)
     check_attention(o, ref, what, weighted_abs_v=wabs)
     check_lse(lse, ref_lse, what)
-    if o32 is not None:  # the fp32 output of the same kernels: the benchmark spec's gate, and o is its rounding
+    if o32 is not None:  # the fp32 output of the same kernels: the 1e-2 / 1e-3 gate, and o is its rounding
         check_attention(o32, ref, what + " (fp32 output)", fp32_gate=True)
         # within one bf16 ulp of the fp32 result rounded: the last split to
         # arrive merges the key splits, so their fp32 summation order varies
