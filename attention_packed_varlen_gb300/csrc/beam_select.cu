@@ -1306,10 +1306,11 @@ cudaError_t launch_beam_select(const void* logits, const float* cum, int W_in, i
   auto* select = p.fused ? sel::select_kernel<true> : sel::select_kernel<false>;
   e = cudaFuncSetAttribute(select, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_sel));
   if (e != cudaSuccess) return e;
-  // Narrow selections re-read a few hundred sub-chunks: 32 CTAs do it as fast
-  // as a CTA per SM and reach the last-CTA ranking sooner (measured 22.5 ->
-  // 21.9 us at W = 100); wide ones keep a CTA per SM.
-  cfg.gridDim = dim3(p.K <= 256 ? std::min(32, sm_count()) : sm_count());
+  // One CTA per SM.  (With the row kernel a narrow selection ran faster on 32
+  // CTAs; with the row statistics in the select kernel, more CTAs finish the
+  // re-read sooner: 18.3 against 19.3 us at W = 100, 13.4 against 15.0 us on
+  // its first step.)
+  cfg.gridDim = dim3(sm_count());
   cfg.blockDim = dim3(sel::kSelThreads);
   cfg.dynamicSmemBytes = smem_sel;
   return cudaLaunchKernelEx(&cfg, select, p);
